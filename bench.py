@@ -1,0 +1,431 @@
+#!/usr/bin/env python
+"""Benchmark of tree-verify attention over a paged MLA latent pool (one GB300).
+
+Metric: verify-attention microseconds per call, with TFLOP/s, KV GB/s and the
+fraction of the roofline max(FLOPs / bf16 peak, bytes / HBM bandwidth).
+
+One step = one full call of the hot path (status clear, split kernel, split
+combine) on one batch of the headline workload, inputs resident in HBM.  L2
+is flushed (a 256 MiB write) before every timed call; each call is timed with
+CUDA events on its own stream.  Prints ONE JSON line.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                  [--config ragged|long|mid|short|tiny] [--kernel tc|simt]
+
+Under torchrun (N > 1) every rank runs an independent replica of the same
+workload (this path has no cross-GPU exchange); the value is the whole-job
+time per call, max over ranks.  ``--impl reference`` times the CPU oracle on
+the host cores (rank 0 only).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "verify-attn µs/call, TFLOP/s and KV GB/s as % of GB300 roofline (1 GPU)"
+UNIT = "us/call"
+HEADLINE = "ragged"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+L2_FLUSH_BYTES = 256 << 20
+KERNEL_SOURCES = {"tc": "speculative_decode_mla_paged_gb300/csrc/verify_tc.cu",
+                  "simt": "speculative_decode_mla_paged_gb300/csrc/verify_simt.cu"}
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--config", default=HEADLINE)
+    ap.add_argument("--kernel", choices=["tc", "simt"], default="tc")
+    ap.add_argument("--num-splits", type=int, default=0, help="0 = per-config default")
+    ap.add_argument("--no-per-config", action="store_true", help="skip the five-config table")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0, help="oracle sample budget")
+    return ap.parse_args()
+
+
+# ------------------------------------------------------------------ helpers
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return {k: float(d[k]) for k in FALLBACK_PEAKS if k in d}, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def default_splits(cfg_name, inp, kernel):
+    """Split count that fills 152 SMs for this workload's grid."""
+    from speculative_decode_mla_paged_gb300 import tuning
+    return tuning.default_num_splits(inp.batch, inp.max_q_per_req, inp.num_heads,
+                                     int(max(inp.prefix_lens + inp.draft_lens)), kernel)
+
+
+def kernel_hash(kernel):
+    with open(os.path.join(ROOT, KERNEL_SOURCES[kernel]), "rb") as f:
+        return hashlib.sha1(f.read()).hexdigest()[:12]
+
+
+def profiled_traffic(kernel, cfg_name):
+    """DRAM bytes per launch from a committed ncu summary for this exact kernel source."""
+    path = os.path.join(ROOT, "profiles", "dram_traffic.md")
+    if not os.path.exists(path):
+        return None
+    h = kernel_hash(kernel)
+    for line in open(path):
+        m = re.match(r"\|\s*(\w+)\s*\|\s*(\w+)\s*\|\s*([0-9a-f]{12})\s*\|\s*([0-9.e+]+)\s*\|", line)
+        if m and m.group(1) == kernel and m.group(2) == cfg_name and m.group(3) == h:
+            return float(m.group(4))
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi clocks / throttle reasons sampled every 200 ms during the timed region."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu_index = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "200"]
+        if self.gpu_index is not None:
+            cmd += ["-i", str(self.gpu_index)]
+        try:
+            self.proc = subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append((time.time(), line.strip()))
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for _, line in self.lines:
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1])); mx.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def dist_setup(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+# ------------------------------------------------------------------ oracle (CPU) timing
+
+def visible_per_row(inp):
+    """Visible keys of every output row (t*H + h), from the packed mask."""
+    bits = np.unpackbits(inp.custom_mask, bitorder="little")
+    counts = []
+    for b in range(inp.batch):
+        T = int(inp.draft_lens[b]); N = int(inp.prefix_lens[b]) + T
+        m0 = int(inp.mask_indptr[b])
+        rows = bits[m0:m0 + T * N].reshape(T, N).sum(axis=1) if T else np.zeros(0)
+        counts.append(np.repeat(rows, inp.num_heads))
+    return np.concatenate(counts).astype(np.int64)
+
+
+def time_oracle(inp, seconds, seed=0):
+    """Run the oracle on a row sample sized to ~`seconds` of CPU work and scale
+    to microseconds per full call by visible (row, key) pairs."""
+    import oracle
+    vis = visible_per_row(inp)
+    total_pairs = float(vis.sum())
+    rng = np.random.default_rng(seed)
+    order = rng.permutation(len(vis))
+    t0 = time.perf_counter()
+    oracle.run(inp, rows=order[:1])
+    one = max(time.perf_counter() - t0, 1e-4)
+    per_pair = one / max(vis[order[0]], 1) / max(1, oracle.num_threads())
+    want_pairs = seconds / per_pair
+    csum = np.cumsum(vis[order])
+    n = int(min(len(vis), max(oracle.num_threads(), np.searchsorted(csum, want_pairs) + 1)))
+    rows = np.sort(order[:n])
+    t0 = time.perf_counter()
+    oracle.run(inp, rows=rows)
+    dt = time.perf_counter() - t0
+    pairs = float(vis[rows].sum())
+    us_per_call = dt * 1e6 * total_pairs / max(pairs, 1.0)
+    return us_per_call, {"rows": int(n), "of_rows": int(len(vis)), "seconds": round(dt, 3),
+                         "pairs": int(pairs), "of_pairs": int(total_pairs)}
+
+
+def run_reference(args):
+    """The oracle, as it stands, on the host cores: K timed steps of a bounded sample."""
+    world, rank, _ = dist_setup(args)
+    if rank != 0:
+        return
+    import oracle
+    from speculative_decode_mla_paged_gb300 import workloads as W
+    oracle.build()
+    inp = W.make_config_inputs(args.config, device="cpu") if args.config in ("tiny", "short") else None
+    if inp is None:
+        import torch
+        if torch.cuda.is_available():
+            inp = W.make_config_inputs(args.config, device="cuda")
+            inp.q, inp.kv_pool = inp.q.cpu(), inp.kv_pool.cpu()
+        else:
+            inp = W.make_config_inputs(args.config, device="cpu")
+    per_step = max(2.0, min(20.0, 150.0 / max(1, args.steps + args.warmup)))
+    for w in range(args.warmup):
+        time_oracle(inp, per_step / 4, seed=1000 + w)
+    vals, samples = [], []
+    for k in range(args.steps):
+        v, s = time_oracle(inp, per_step, seed=k)
+        vals.append(v); samples.append(s)
+    value = statistics.mean(vals)
+    cores = oracle.num_threads()
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": value / 1e3,
+        "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": {"workload": W.CONFIGS[args.config].description,
+                                        "name": args.config},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
+                         "sample": f"per step {samples[0]['rows']} of {samples[0]['of_rows']} output rows "
+                                   f"({statistics.mean(s['seconds'] for s in samples):.2f} s, budget "
+                                   f"{per_step:.0f} s), scaled to a full call by visible (row, key) pairs"},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ------------------------------------------------------------------ our arm
+
+def measure(inp, d, runner, steps, warmup, flush, torch):
+    """Device timing of `steps` calls, each after an L2 flush.  Returns per-step
+    lists of (call_ms, split_ms, combine_ms)."""
+    from speculative_decode_mla_paged_gb300 import api  # noqa: F401
+    out = d["out"]
+    stream = torch.cuda.current_stream()
+
+    def call(events=None):
+        runner(d["q"], d["kv_pool"], d["qo_indptr"], d["kv_indptr"], d["kv_indices"], d["out_cache_loc"],
+               d["custom_mask"], d["mask_indptr"], inp.sm_scale, out, events=events)
+
+    for _ in range(warmup):
+        flush.zero_()
+        call()
+    torch.cuda.synchronize()
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(steps)]
+    for k in range(steps):
+        flush.zero_()
+        call(evs[k])
+    torch.cuda.synchronize()
+    call_ms = [e[0].elapsed_time(e[3]) for e in evs]
+    split_ms = [e[1].elapsed_time(e[2]) for e in evs]
+    comb_ms = [e[2].elapsed_time(e[3]) for e in evs]
+    return call_ms, split_ms, comb_ms
+
+
+def device_tensors(inp, torch, dev):
+    from speculative_decode_mla_paged_gb300 import api  # noqa: F401
+    d = {k: torch.from_numpy(np.ascontiguousarray(getattr(inp, k))).to(dev)
+         for k in ("qo_indptr", "kv_indptr", "kv_indices", "out_cache_loc", "custom_mask", "mask_indptr")}
+    d["q"] = inp.q.to(dev)
+    d["kv_pool"] = inp.kv_pool.to(dev)
+    d["out"] = torch.empty(inp.total_q, inp.num_heads, 512, dtype=torch.bfloat16, device=dev)
+    return d
+
+
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+
+    from speculative_decode_mla_paged_gb300 import api
+    from speculative_decode_mla_paged_gb300 import workloads as W
+
+    world, rank, local = dist_setup(args)
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=dev)
+    api.init()
+    peaks, peak_src = load_peaks()
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+
+    inp = W.make_config_inputs(args.config, device=dev)
+    splits = args.num_splits or default_splits(args.config, inp, args.kernel)
+    d = device_tensors(inp, torch, dev)
+    runner = api.VerifyAttention(inp.batch, inp.max_q_per_req, inp.num_heads, splits, impl=args.kernel)
+
+    # ---- device-resident timed region
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    gpu_index = None
+    try:
+        vis = os.environ.get("CUDA_VISIBLE_DEVICES")
+        gpu_index = int(vis.split(",")[local]) if vis else local
+    except ValueError:
+        gpu_index = None
+    sampler = ClockSampler(gpu_index)
+    sampler.start()
+    time.sleep(0.3)
+    call_ms, split_ms, comb_ms = measure(inp, d, runner, args.steps, args.warmup, flush, torch)
+    clocks = sampler.stop()
+    status = runner.status()
+    if status != 0:
+        raise RuntimeError(f"device status word {status:#x}")
+    total = torch.tensor([sum(call_ms)], dtype=torch.float64, device=dev)
+    if world > 1:
+        dist.all_reduce(total, op=dist.ReduceOp.MAX)
+    t_total_ms = float(total.item())
+    value_us = t_total_ms * 1e3 / (args.steps * world)
+
+    # ---- end-to-end: pinned host inputs -> device, call, result -> host
+    h2d_names = ("q", "qo_indptr", "kv_indptr", "kv_indices", "out_cache_loc", "custom_mask", "mask_indptr")
+    host = {k: (inp.q.cpu() if k == "q" else torch.from_numpy(np.ascontiguousarray(getattr(inp, k)))).pin_memory()
+            for k in h2d_names}
+    host_out = torch.empty(d["out"].shape, dtype=torch.bfloat16).pin_memory()
+    h2d_bytes = sum(t.numel() * t.element_size() for t in host.values())
+    d2h_bytes = host_out.numel() * host_out.element_size()
+    e2e_ms = []
+    for k in range(args.warmup + args.steps):
+        flush.zero_()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for name in h2d_names:
+            d[name].copy_(host[name], non_blocking=True)
+        runner(d["q"], d["kv_pool"], d["qo_indptr"], d["kv_indptr"], d["kv_indices"], d["out_cache_loc"],
+               d["custom_mask"], d["mask_indptr"], inp.sm_scale, d["out"])
+        host_out.copy_(d["out"], non_blocking=True)
+        e1.record()
+        e1.synchronize()
+        if k >= args.warmup:
+            e2e_ms.append(e0.elapsed_time(e1))
+    e2e_total = torch.tensor([sum(e2e_ms)], dtype=torch.float64, device=dev)
+    if world > 1:
+        dist.all_reduce(e2e_total, op=dist.ReduceOp.MAX)
+    e2e_us = float(e2e_total.item()) * 1e3 / (args.steps * world)
+
+    # ---- roofline of the dominant kernel (the split kernel)
+    flops = inp.algorithmic_flops()
+    nbytes = inp.algorithmic_bytes()
+    split_s = statistics.mean(split_ms) / 1e3
+    call_s = statistics.mean(call_ms) / 1e3
+    t_f = flops / (peaks["bf16_tflops"] * 1e12)
+    t_b = nbytes / (peaks["hbm_gbs"] * 1e9)
+    if t_f >= t_b:
+        roof = {"bound": "tensor", "achieved": flops / split_s / 1e12, "peak": peaks["bf16_tflops"],
+                "unit": "TFLOP/s"}
+    else:
+        roof = {"bound": "hbm", "achieved": nbytes / split_s / 1e9, "peak": peaks["hbm_gbs"], "unit": "GB/s"}
+    roof["frac"] = roof["achieved"] / roof["peak"]
+    roof["traffic"] = profiled_traffic(args.kernel, args.config)
+    roof["peak_source"] = f"{peak_src} (burst; kernel timed alone)"
+    roof["kernel"] = f"{args.kernel} split kernel"
+    roof["algorithmic_flops"] = flops
+    roof["algorithmic_bytes"] = nbytes
+
+    line = {
+        "metric": METRIC, "value": value_us, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": t_total_ms / args.steps, "higher_is_better": False,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": f"{args.config}: {W.CONFIGS[args.config].description}",
+                   "kernel": args.kernel, "num_splits": splits,
+                   "l2": "flushed before every timed call (256 MiB write, excluded from timing)",
+                   "parallelism": "replicas" if world > 1 else "single-gpu"},
+        "tflops": flops / call_s / 1e12, "kv_gbs": nbytes / call_s / 1e9,
+        "roofline_frac_call": max(t_f, t_b) / call_s,
+        "split_us": statistics.mean(split_ms) * 1e3, "combine_us": statistics.mean(comb_ms) * 1e3,
+        "roofline": roof,
+        "e2e": {"value": e2e_us, "unit": UNIT, "h2d_bytes_per_step": int(h2d_bytes),
+                "d2h_bytes_per_step": int(d2h_bytes)},
+        "gpu_launches": 2 * args.steps,
+        "clocks": clocks,
+    }
+
+    # ---- the five workloads, device time per call (informational)
+    if rank == 0 and not args.no_per_config:
+        table = {}
+        for name in W.CONFIG_ORDER:
+            ci = inp if name == args.config else W.make_config_inputs(name, device=dev)
+            cs = args.num_splits or default_splits(name, ci, args.kernel)
+            cd = d if name == args.config else device_tensors(ci, torch, dev)
+            cr = runner if name == args.config else api.VerifyAttention(ci.batch, ci.max_q_per_req,
+                                                                          ci.num_heads, cs, impl=args.kernel)
+            cm, sm, _ = measure(ci, cd, cr, 5, 3, flush, torch)
+            f, b = ci.algorithmic_flops(), ci.algorithmic_bytes()
+            tc = statistics.mean(cm) / 1e3
+            table[name] = {"us_per_call": tc * 1e6, "split_us": statistics.mean(sm) * 1e3,
+                           "tflops": f / tc / 1e12, "kv_gbs": b / tc / 1e9,
+                           "roofline_frac": max(f / (peaks["bf16_tflops"] * 1e12),
+                                                b / (peaks["hbm_gbs"] * 1e9)) / tc,
+                           "num_splits": cs}
+            if name != args.config:
+                del cd, cr, ci
+                torch.cuda.empty_cache()
+        line["per_config"] = table
+
+    # ---- CPU oracle baseline on the host cores (rank 0, N = 1 only)
+    if rank == 0 and world == 1:
+        import oracle
+        oracle.build()
+        inp.q, inp.kv_pool = inp.q.cpu(), inp.kv_pool.cpu()
+        us, sample = time_oracle(inp, args.cpu_seconds)
+        line["cpu_baseline"] = {"value": us, "unit": UNIT, "cores": oracle.num_threads(), "kind": "oracle",
+                                "sample": f"{sample['rows']} of {sample['of_rows']} output rows "
+                                          f"({sample['seconds']} s), scaled to a full call by visible "
+                                          "(row, key) pairs"}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def main():
+    args = parse_args()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,199 @@
+/*
+ * verify_attn.h -- C ABI of libverify_attn: tree-verify attention for
+ * speculative decoding over a paged MLA latent KV pool (page_size = 1), for
+ * NVIDIA GB300 (sm_103a).
+ *
+ * The operation ("The Capture-Safe Kernel", sections The Core Problem and
+ * The Design Decisions; "The Integration Chasm", sections Decision and
+ * Subject Message; "The Launch Wrapper", section Input):
+ *
+ *   For request b of a ragged batch, T_b = qo_indptr[b+1]-qo_indptr[b] draft
+ *   tokens x H heads attend to N_b = L_b + T_b keys, L_b =
+ *   kv_indptr[b+1]-kv_indptr[b] (derived in-kernel, Decision 2).  Key j < L_b
+ *   is pool row kv_indices[kv_indptr[b]+j]; key j >= L_b is draft token
+ *   j-L_b, pool row out_cache_loc[qo_indptr[b]+j-L_b] (Decision 1: native
+ *   buffers read in place).  Draft i sees key j iff bit mask_indptr[b] +
+ *   i*N_b + j of custom_mask is set (Decision 5), LSB-first in each byte.
+ *   With K_j = pool[slot_j, 0:576] and V_j = pool[slot_j, 0:512] (MLA latent
+ *   attention after absorption: 512 no-PE + 64 RoPE dims per row, V = the
+ *   no-PE part):
+ *       out[t, h, :] = softmax_j( sm_scale * <q[t,h,:], K_j> ) . V_j
+ *   over the visible j.  A row with no visible key gets zeros.
+ *
+ *   The library computes it as split-KV flash-decode ("The Integration
+ *   Chasm", section Context: KV-split partial-plus-reduce; "The Capture-Safe
+ *   Kernel", Decision 3): each split covers a contiguous key chunk and writes
+ *   a partial output plus its log-sum-exp into the workspace; a second
+ *   kernel merges the partials.
+ *
+ * Contract of every entry point that takes a stream:
+ *   - all tensor pointers are DEVICE pointers owned by the caller;
+ *   - the library keeps no per-call state, allocates nothing, never
+ *     synchronises, and launches only on `stream` (0 = legacy default
+ *     stream), so a call can be captured into a CUDA graph and replayed
+ *     after the caller rewrites the *contents* of its buffers (Decision 6:
+ *     no replay-metadata hook needed);
+ *   - host-side argument errors are reported by a negative VA_ERR_* return
+ *     and nothing is launched;
+ *   - device-side data errors never trap: a slot id outside [0, pool_size)
+ *     (or a null index buffer that a request needs) makes the kernel skip
+ *     that key and OR bit VA_STATUS_BAD_SLOT into the 32-bit status word at
+ *     byte 0 of the workspace; each run clears that word first.  The caller
+ *     reads it after its own synchronisation.
+ *
+ * Thread safety: calls may be made from several host threads; concurrent
+ * calls must use distinct workspaces.
+ */
+#ifndef VERIFY_ATTN_H
+#define VERIFY_ATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Symbols of this header are the library's only exported names. */
+#if defined(__GNUC__)
+#define VERIFY_ATTN_API __attribute__((visibility("default")))
+#else
+#define VERIFY_ATTN_API
+#endif
+
+/* Opaque CUDA stream handle (the same object as cudaStream_t / CUstream). */
+typedef struct CUstream_st *verify_attn_stream_t;
+
+/* Fixed latent geometry: 576-wide rows (512 no-PE + 64 RoPE), V = first 512. */
+#define VERIFY_ATTN_LATENT_DIM 576
+#define VERIFY_ATTN_V_DIM 512
+/* Upper bound on num_splits accepted by the run entry points. */
+#define VERIFY_ATTN_MAX_SPLITS 256
+
+enum verify_attn_status {
+    VA_OK = 0,
+    VA_ERR_NULL = -1,       /* a required pointer is null                          */
+    VA_ERR_ALIGN = -2,      /* q/kv_pool/out not 16-B aligned, strides not x8 elems,
+                               or workspace not 256-B aligned                        */
+    VA_ERR_DIMS = -3,       /* batch/heads/max_q_per_req/pool_size out of range     */
+    VA_ERR_WORKSPACE = -4,  /* workspace_bytes < verify_attn_workspace_size(...)   */
+    VA_ERR_SPLITS = -5,     /* num_splits outside [1, VERIFY_ATTN_MAX_SPLITS]       */
+    VA_ERR_LAUNCH = -6,     /* a CUDA launch or attribute call failed               */
+    VA_ERR_SCALE = -7,      /* sm_scale not finite                                   */
+    VA_ERR_DEVICE = -8,     /* the current device is not sm_103 or cannot be queried */
+};
+
+/* Bits of the device status word (workspace byte 0). */
+#define VA_STATUS_BAD_SLOT 0x1u   /* slot outside [0,pool_size) or null index buffer */
+#define VA_STATUS_BAD_META 0x2u   /* some T_b > max_q_per_req, or negative lengths;
+                                     rows past the capacity are not computed        */
+
+/*
+ * Workspace bytes needed by verify_attn_run / verify_attn_run_simt for a
+ * call with these capacities: a 256-B header (status word), then fp32 split
+ * partials [num_splits][batch*max_q_per_req*num_heads][512] and their
+ * log-sum-exp [num_splits][batch*max_q_per_req*num_heads].  The caller
+ * allocates it (e.g. torch.empty(..., dtype=uint8, device="cuda")) --
+ * "The Capture-Safe Kernel", Decision 4: workspace as a caller tensor, not a
+ * raw cudaMalloc.  Returns 0 for invalid capacities.
+ */
+VERIFY_ATTN_API size_t verify_attn_workspace_size(int batch, int max_q_per_req, int num_heads, int num_splits);
+
+/*
+ * One-time per-device setup for the current device (kernel attributes such
+ * as the dynamic shared-memory limit).  verify_attn_run calls it lazily, but
+ * callers that capture CUDA graphs should call it once before capturing.
+ * Returns VA_OK, VA_ERR_DEVICE or VA_ERR_LAUNCH.
+ */
+VERIFY_ATTN_API int verify_attn_init(void);
+
+/*
+ * Tree-verify attention, production path (tensor-core split kernel on
+ * sm_103a, then the log-sum-exp combine).
+ *
+ *   q            [sum T_b, H, 576] bf16; element (t,h,d) at
+ *                q[t*q_stride_tok + h*q_stride_head + d]; strides in
+ *                elements, multiples of 8; 16-B aligned base.
+ *   kv_pool      [pool_size, 576] bf16, rows contiguous (1152 B), 16-B aligned.
+ *   qo_indptr    [batch+1] int32, non-decreasing, qo_indptr[0] = 0, every
+ *                T_b <= max_q_per_req.
+ *   kv_indptr    [batch+1] int32, non-decreasing, kv_indptr[0] = 0 (prefix keys).
+ *   kv_indices   [kv_indptr[batch]] int32 pool slots of the prefix keys.
+ *   out_cache_loc[qo_indptr[batch]] int64 pool slots of the draft tokens.
+ *   custom_mask  packed visibility bits (layout above).
+ *   mask_indptr  [batch+1] int64 bit offsets; mask_indptr[b+1]-mask_indptr[b]
+ *                = T_b*(L_b+T_b).
+ *   sm_scale     softmax scale applied to <q, K> (e.g. 1/sqrt(192)).
+ *   out          [sum T_b, H, 512] bf16 (round to nearest even), strides like q.
+ *   batch, max_q_per_req, num_heads, num_splits: host capacities that fix
+ *                the launch grid (so one captured graph serves every batch
+ *                with these bounds).  Request b's keys are cut into chunks of
+ *                c_b = ceil(N_b/num_splits) rounded up to a multiple of 64;
+ *                splits past the end exit at once (Decision 3).
+ *   workspace    device scratch of workspace_bytes (see above), 256-B aligned.
+ *
+ * The index buffers and the mask are read in place, inside the kernels; the
+ * call allocates nothing and does not synchronise.  Returns VA_OK or a
+ * negative VA_ERR_*.
+ */
+VERIFY_ATTN_API int verify_attn_run(const void *q, int64_t q_stride_tok, int64_t q_stride_head,
+                                    const void *kv_pool, int64_t pool_size,
+                                    const int32_t *qo_indptr, const int32_t *kv_indptr,
+                                    const int32_t *kv_indices, const int64_t *out_cache_loc,
+                                    const uint8_t *custom_mask, const int64_t *mask_indptr,
+                                    float sm_scale,
+                                    void *out, int64_t out_stride_tok, int64_t out_stride_head,
+                                    int batch, int max_q_per_req, int num_heads, int num_splits,
+                                    void *workspace, size_t workspace_bytes,
+                                    verify_attn_stream_t stream);
+
+/*
+ * Same operation and arguments on the portable CUDA-core kernel (fp32 FMA,
+ * no tensor cores).  It is the side-by-side cross-check of the production
+ * kernel on live buffers, in the spirit of the pages' "validate" mode ("The
+ * Launch Wrapper", section The Design Decision: Three Modes of Operation).
+ */
+VERIFY_ATTN_API int verify_attn_run_simt(const void *q, int64_t q_stride_tok, int64_t q_stride_head,
+                                         const void *kv_pool, int64_t pool_size,
+                                         const int32_t *qo_indptr, const int32_t *kv_indptr,
+                                         const int32_t *kv_indices, const int64_t *out_cache_loc,
+                                         const uint8_t *custom_mask, const int64_t *mask_indptr,
+                                         float sm_scale,
+                                         void *out, int64_t out_stride_tok, int64_t out_stride_head,
+                                         int batch, int max_q_per_req, int num_heads, int num_splits,
+                                         void *workspace, size_t workspace_bytes,
+                                         verify_attn_stream_t stream);
+
+/* Kernel selectors for verify_attn_run_profiled. */
+#define VERIFY_ATTN_IMPL_TC 0     /* the verify_attn_run path   */
+#define VERIFY_ATTN_IMPL_SIMT 1   /* the verify_attn_run_simt path */
+
+/*
+ * verify_attn_run (impl = VERIFY_ATTN_IMPL_TC) or verify_attn_run_simt
+ * (VERIFY_ATTN_IMPL_SIMT) with timing marks: events[0..3] are cudaEvent_t
+ * handles created by the caller (any may be null), recorded on `stream`
+ * at the start of the call, just before the split kernel (after the status
+ * word is cleared), between the split kernel and the combine, and after the
+ * combine.  Lets a caller time each of the two kernels on the stream they
+ * run on.  Same return codes; an unknown impl gives VA_ERR_DIMS.
+ */
+VERIFY_ATTN_API int verify_attn_run_profiled(int impl, void *const *events,
+                                             const void *q, int64_t q_stride_tok, int64_t q_stride_head,
+                                             const void *kv_pool, int64_t pool_size,
+                                             const int32_t *qo_indptr, const int32_t *kv_indptr,
+                                             const int32_t *kv_indices, const int64_t *out_cache_loc,
+                                             const uint8_t *custom_mask, const int64_t *mask_indptr,
+                                             float sm_scale,
+                                             void *out, int64_t out_stride_tok, int64_t out_stride_head,
+                                             int batch, int max_q_per_req, int num_heads, int num_splits,
+                                             void *workspace, size_t workspace_bytes,
+                                             verify_attn_stream_t stream);
+
+/* Short English description of a VA_* status code (static storage). */
+VERIFY_ATTN_API const char *verify_attn_status_string(int status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* VERIFY_ATTN_H */

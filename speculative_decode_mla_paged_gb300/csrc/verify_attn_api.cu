@@ -1,0 +1,211 @@
+// Host side of the C ABI declared in include/verify_attn.h: argument
+// checks, workspace carving, per-device one-time setup and the launches.
+// Nothing here allocates device memory or synchronises ("The Capture-Safe
+// Kernel", section The Core Problem: host syncs, raw cudaMalloc and
+// temporaries are what break graph capture).
+#include "verify_attn.h"
+#include "va_internal.cuh"
+
+#include <atomic>
+#include <math.h>
+
+namespace va {
+
+cudaError_t tc_init();
+cudaError_t launch_tc_split(const Params &p, cudaStream_t stream);
+bool tc_supported(const Params &p);
+
+namespace {
+
+std::atomic<uint64_t> g_init_mask{0};   // bit d: device d initialised
+
+int ensure_init()
+{
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return VA_ERR_DEVICE;
+    const uint64_t bit = 1ull << dev;
+    if (g_init_mask.load(std::memory_order_acquire) & bit) return VA_OK;
+    int major = 0, minor = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
+        return VA_ERR_DEVICE;
+    if (major != 10 || minor != 3) return VA_ERR_DEVICE;   // built for sm_103a only
+    if (simt_init() != cudaSuccess) return VA_ERR_LAUNCH;
+    if (tc_init() != cudaSuccess) return VA_ERR_LAUNCH;
+    g_init_mask.fetch_or(bit, std::memory_order_acq_rel);
+    return VA_OK;
+}
+
+bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+size_t ws_size(int batch, int max_q, int heads, int splits)
+{
+    if (batch < 0 || max_q < 0 || heads <= 0 || splits < 1 || splits > VERIFY_ATTN_MAX_SPLITS)
+        return 0;
+    const size_t rows = (size_t)batch * (size_t)max_q * (size_t)heads;
+    const size_t o_bytes = (size_t)splits * rows * DV * sizeof(float);
+    const size_t lse_bytes = (size_t)splits * rows * sizeof(float);
+    return WS_HEADER + o_bytes + ((lse_bytes + 255) & ~(size_t)255);
+}
+
+// Validate host arguments and fill Params.  Returns VA_OK or VA_ERR_*.
+int prepare(Params &p, const void *q, int64_t q_st, int64_t q_sh, const void *kv_pool,
+            int64_t pool_size, const int32_t *qo_indptr, const int32_t *kv_indptr,
+            const int32_t *kv_indices, const int64_t *out_cache_loc, const uint8_t *custom_mask,
+            const int64_t *mask_indptr, float sm_scale, void *out, int64_t o_st, int64_t o_sh,
+            int batch, int max_q, int heads, int splits, void *workspace, size_t ws_bytes)
+{
+    if (!q || !kv_pool || !qo_indptr || !kv_indptr || !custom_mask || !mask_indptr || !out ||
+        !workspace)
+        return VA_ERR_NULL;
+    if (batch < 0 || max_q < 0 || heads <= 0 || pool_size <= 0) return VA_ERR_DIMS;
+    if ((int64_t)batch * max_q * heads > (int64_t)1 << 31) return VA_ERR_DIMS;
+    if (splits < 1 || splits > VERIFY_ATTN_MAX_SPLITS) return VA_ERR_SPLITS;
+    if (!isfinite(sm_scale)) return VA_ERR_SCALE;
+    if (!aligned(q, 16) || !aligned(kv_pool, 16) || !aligned(out, 16) || !aligned(workspace, 256))
+        return VA_ERR_ALIGN;
+    if ((q_st | q_sh | o_st | o_sh) & 7) return VA_ERR_ALIGN;
+    if (q_st < 0 || q_sh < 0 || o_st < 0 || o_sh < 0) return VA_ERR_ALIGN;
+    const size_t need = ws_size(batch, max_q, heads, splits);
+    if (need == 0) return VA_ERR_DIMS;
+    if (ws_bytes < need) return VA_ERR_WORKSPACE;
+
+    p.q = static_cast<const __nv_bfloat16 *>(q);
+    p.q_stride_tok = q_st;
+    p.q_stride_head = q_sh;
+    p.kv_pool = static_cast<const __nv_bfloat16 *>(kv_pool);
+    p.pool_size = pool_size;
+    p.qo_indptr = qo_indptr;
+    p.kv_indptr = kv_indptr;
+    p.kv_indices = kv_indices;
+    p.out_cache_loc = out_cache_loc;
+    p.custom_mask = custom_mask;
+    p.mask_indptr = mask_indptr;
+    p.sm_scale = sm_scale;
+    p.out = static_cast<__nv_bfloat16 *>(out);
+    p.out_stride_tok = o_st;
+    p.out_stride_head = o_sh;
+    p.batch = batch;
+    p.max_q_per_req = max_q;
+    p.num_heads = heads;
+    p.num_splits = splits;
+    p.rows_cap = (int64_t)batch * max_q * heads;
+    unsigned char *ws = static_cast<unsigned char *>(workspace);
+    p.status = reinterpret_cast<unsigned *>(ws);
+    p.part_o = reinterpret_cast<float *>(ws + WS_HEADER);
+    p.part_lse = reinterpret_cast<float *>(ws + WS_HEADER + (size_t)splits * p.rows_cap * DV * sizeof(float));
+    return VA_OK;
+}
+
+enum class Impl { Tc, Simt };
+
+int run(Impl impl, const void *q, int64_t q_st, int64_t q_sh, const void *kv_pool,
+        int64_t pool_size, const int32_t *qo_indptr, const int32_t *kv_indptr,
+        const int32_t *kv_indices, const int64_t *out_cache_loc, const uint8_t *custom_mask,
+        const int64_t *mask_indptr, float sm_scale, void *out, int64_t o_st, int64_t o_sh,
+        int batch, int max_q, int heads, int splits, void *workspace, size_t ws_bytes,
+        verify_attn_stream_t stream, cudaEvent_t const *events = nullptr)
+{
+    Params p;
+    int rc = prepare(p, q, q_st, q_sh, kv_pool, pool_size, qo_indptr, kv_indptr, kv_indices,
+                     out_cache_loc, custom_mask, mask_indptr, sm_scale, out, o_st, o_sh, batch,
+                     max_q, heads, splits, workspace, ws_bytes);
+    if (rc != VA_OK) return rc;
+    rc = ensure_init();
+    if (rc != VA_OK) return rc;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    auto mark = [&](int k) {
+        return events == nullptr || events[k] == nullptr || cudaEventRecord(events[k], s) == cudaSuccess;
+    };
+    if (!mark(0)) return VA_ERR_LAUNCH;
+    if (cudaMemsetAsync(p.status, 0, sizeof(unsigned), s) != cudaSuccess) return VA_ERR_LAUNCH;
+    if (!mark(1)) return VA_ERR_LAUNCH;
+    cudaError_t e = cudaSuccess;
+    if (p.rows_cap > 0) {
+        if (impl == Impl::Tc && tc_supported(p))
+            e = launch_tc_split(p, s);
+        else
+            e = launch_simt_split(p, s);
+    }
+    if (e != cudaSuccess || !mark(2)) return VA_ERR_LAUNCH;
+    if (p.rows_cap > 0 && launch_combine(p, s) != cudaSuccess) return VA_ERR_LAUNCH;
+    if (!mark(3)) return VA_ERR_LAUNCH;
+    return VA_OK;
+}
+
+}  // namespace
+}  // namespace va
+
+extern "C" {
+
+size_t verify_attn_workspace_size(int batch, int max_q_per_req, int num_heads, int num_splits)
+{
+    return va::ws_size(batch, max_q_per_req, num_heads, num_splits);
+}
+
+int verify_attn_init(void) { return va::ensure_init(); }
+
+int verify_attn_run(const void *q, int64_t q_stride_tok, int64_t q_stride_head, const void *kv_pool,
+                    int64_t pool_size, const int32_t *qo_indptr, const int32_t *kv_indptr,
+                    const int32_t *kv_indices, const int64_t *out_cache_loc,
+                    const uint8_t *custom_mask, const int64_t *mask_indptr, float sm_scale,
+                    void *out, int64_t out_stride_tok, int64_t out_stride_head, int batch,
+                    int max_q_per_req, int num_heads, int num_splits, void *workspace,
+                    size_t workspace_bytes, verify_attn_stream_t stream)
+{
+    return va::run(va::Impl::Tc, q, q_stride_tok, q_stride_head, kv_pool, pool_size, qo_indptr,
+                   kv_indptr, kv_indices, out_cache_loc, custom_mask, mask_indptr, sm_scale, out,
+                   out_stride_tok, out_stride_head, batch, max_q_per_req, num_heads, num_splits,
+                   workspace, workspace_bytes, stream);
+}
+
+int verify_attn_run_simt(const void *q, int64_t q_stride_tok, int64_t q_stride_head,
+                         const void *kv_pool, int64_t pool_size, const int32_t *qo_indptr,
+                         const int32_t *kv_indptr, const int32_t *kv_indices,
+                         const int64_t *out_cache_loc, const uint8_t *custom_mask,
+                         const int64_t *mask_indptr, float sm_scale, void *out,
+                         int64_t out_stride_tok, int64_t out_stride_head, int batch,
+                         int max_q_per_req, int num_heads, int num_splits, void *workspace,
+                         size_t workspace_bytes, verify_attn_stream_t stream)
+{
+    return va::run(va::Impl::Simt, q, q_stride_tok, q_stride_head, kv_pool, pool_size, qo_indptr,
+                   kv_indptr, kv_indices, out_cache_loc, custom_mask, mask_indptr, sm_scale, out,
+                   out_stride_tok, out_stride_head, batch, max_q_per_req, num_heads, num_splits,
+                   workspace, workspace_bytes, stream);
+}
+
+int verify_attn_run_profiled(int impl, void *const *events, const void *q, int64_t q_stride_tok,
+                             int64_t q_stride_head, const void *kv_pool, int64_t pool_size,
+                             const int32_t *qo_indptr, const int32_t *kv_indptr,
+                             const int32_t *kv_indices, const int64_t *out_cache_loc,
+                             const uint8_t *custom_mask, const int64_t *mask_indptr,
+                             float sm_scale, void *out, int64_t out_stride_tok,
+                             int64_t out_stride_head, int batch, int max_q_per_req, int num_heads,
+                             int num_splits, void *workspace, size_t workspace_bytes,
+                             verify_attn_stream_t stream)
+{
+    if (impl != VERIFY_ATTN_IMPL_TC && impl != VERIFY_ATTN_IMPL_SIMT) return VA_ERR_DIMS;
+    return va::run(impl == VERIFY_ATTN_IMPL_TC ? va::Impl::Tc : va::Impl::Simt, q, q_stride_tok,
+                   q_stride_head, kv_pool, pool_size, qo_indptr, kv_indptr, kv_indices,
+                   out_cache_loc, custom_mask, mask_indptr, sm_scale, out, out_stride_tok,
+                   out_stride_head, batch, max_q_per_req, num_heads, num_splits, workspace,
+                   workspace_bytes, stream, reinterpret_cast<cudaEvent_t const *>(events));
+}
+
+const char *verify_attn_status_string(int status)
+{
+    switch (status) {
+    case VA_OK: return "ok";
+    case VA_ERR_NULL: return "a required pointer is null";
+    case VA_ERR_ALIGN: return "misaligned pointer or stride";
+    case VA_ERR_DIMS: return "batch/heads/max_q_per_req/pool_size out of range";
+    case VA_ERR_WORKSPACE: return "workspace too small";
+    case VA_ERR_SPLITS: return "num_splits out of range";
+    case VA_ERR_LAUNCH: return "CUDA launch failed";
+    case VA_ERR_SCALE: return "sm_scale is not finite";
+    case VA_ERR_DEVICE: return "current device is not sm_103";
+    default: return "unknown status";
+    }
+}
+
+}  // extern "C"

@@ -1,0 +1,268 @@
+"""GPU parity: the CUDA path (through the C ABI) against the CPU oracle."""
+import numpy as np
+import pytest
+import torch
+
+from speculative_decode_mla_paged_gb300 import api
+from speculative_decode_mla_paged_gb300 import workloads as W
+
+from gpu_helpers import as_rows, assert_parity, device_inputs, oracle_rows, run, sample_rows
+
+pytestmark = pytest.mark.gpu
+IMPLS = ["tc", "simt"]
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _init():
+    api.init()
+
+
+# ---------------------------------------------------------------- the five workloads
+
+@pytest.mark.parametrize("impl", IMPLS)
+@pytest.mark.parametrize("name,splits", [("tiny", 1), ("tiny", 4), ("tiny", 64), ("short", 8)])
+def test_small_configs_every_row(name, splits, impl):
+    inp = W.make_config_inputs(name, device="cpu")
+    out, status = run(inp, impl=impl, num_splits=splits)
+    assert status == 0
+    assert_parity(as_rows(out), oracle_rows(inp), f"{name}/{impl}/{splits}")
+
+
+@pytest.mark.parametrize("impl", IMPLS)
+@pytest.mark.parametrize("name,splits", [("mid", 16), ("long", 8), ("ragged", 64)])
+def test_large_configs_sampled_rows(name, splits, impl):
+    """Full-size launch; the oracle checks sampled rows (first/last row of each
+    request plus random ones)."""
+    inp = W.make_config_inputs(name, device="cuda")
+    out, status = run(inp, impl=impl, num_splits=splits)
+    assert status == 0
+    got = as_rows(out)
+    assert np.all(np.isfinite(got))
+    inp_host = inp
+    inp_host.q, inp_host.kv_pool = inp.q.cpu(), inp.kv_pool.cpu()
+    rows = sample_rows(inp_host, n_random=40, seed=hash(name) % 1000)
+    assert_parity(got[rows], oracle_rows(inp_host, rows), f"{name}/{impl}")
+
+
+def test_large_config_kernels_agree_on_every_row():
+    """At full size every row of the tensor-core path matches the CUDA-core
+    path within the same bar (the oracle covers the sampled rows above)."""
+    inp = W.make_config_inputs("mid", device="cuda")
+    d = device_inputs(inp)
+    a, _ = run(inp, impl="tc", num_splits=16, d=d)
+    b, _ = run(inp, impl="simt", num_splits=5, d=d)
+    assert_parity(as_rows(a), as_rows(b), "tc vs simt on mid")
+
+
+# ---------------------------------------------------------------- edge cases
+
+RAGGED_CASES = {
+    # prefix lengths, draft lengths, heads
+    "mixed": ([0, 1, 63, 64, 65, 200], [1, 3, 7, 2, 16, 5], 8),
+    "odd_heads": ([37, 130], [5, 9], 3),
+    "one_head_one_token": ([500], [1], 1),
+    "empty_requests": ([10, 0, 77, 5], [0, 4, 0, 2], 4),
+    "drafts_only": ([0, 0], [6, 11], 8),
+    "many_rows": ([300], [64], 16),
+}
+
+
+@pytest.mark.parametrize("impl", IMPLS)
+@pytest.mark.parametrize("case", sorted(RAGGED_CASES))
+@pytest.mark.parametrize("splits", [1, 3, 256])
+def test_ragged_edge_cases(case, splits, impl):
+    prefix, drafts, H = RAGGED_CASES[case]
+    inp = W.make_inputs(prefix, drafts, H, pool_size=2048, seed=len(prefix) + splits, q_scale=2.0)
+    out, status = run(inp, impl=impl, num_splits=splits, max_q=max(drafts) + 3)
+    assert status == 0
+    if inp.total_q:
+        assert_parity(as_rows(out), oracle_rows(inp), f"{case}/{impl}/{splits}")
+
+
+@pytest.mark.parametrize("impl", IMPLS)
+def test_random_prefix_bits_and_blind_rows(impl):
+    """Prefix bits are read, not assumed: random prefix masks, plus one draft
+    row that sees nothing at all (zeros)."""
+    prefix, drafts, H = [150, 70], [6, 4], 4
+    rng = np.random.default_rng(3)
+    pv = [rng.random((t, l)) < 0.5 for l, t in zip(prefix, drafts)]
+    inp = W.make_inputs(prefix, drafts, H, pool_size=512, seed=3,
+                        extra_prefix_mask=lambda b, t, l: pv[b])
+    bits = np.unpackbits(inp.custom_mask, bitorder="little")[: int(inp.mask_indptr[-1])].copy()
+    N0 = prefix[0] + drafts[0]
+    bits[2 * N0:3 * N0] = 0                      # request 0, draft 2 sees nothing
+    inp.custom_mask = np.packbits(bits, bitorder="little")
+    out, status = run(inp, impl=impl, num_splits=3)
+    assert status == 0
+    got, ref = as_rows(out), oracle_rows(inp)
+    assert np.all(got[2 * H:3 * H] == 0)
+    assert_parity(got, ref, f"random prefix/{impl}")
+
+
+@pytest.mark.parametrize("impl", IMPLS)
+def test_strided_q_and_out(impl):
+    """q and out as views with padded token/head strides (no .contiguous())."""
+    inp = W.make_inputs([90, 33], [7, 3], 4, pool_size=512, seed=21)
+    d = device_inputs(inp)
+    big_q = torch.zeros(inp.total_q, 6, 584, dtype=torch.bfloat16, device="cuda")
+    big_q[:, 1:5, 8:584] = d["q"]
+    d["q"] = big_q[:, 1:5, 8:584]
+    big_out = torch.full((inp.total_q, 5, 520), 7.0, dtype=torch.bfloat16, device="cuda")
+    out = big_out[:, :4, 8:520]
+    run(inp, impl=impl, num_splits=2, d=d, out=out)
+    assert_parity(as_rows(out.contiguous()), oracle_rows(inp), f"strided/{impl}")
+    assert torch.all(big_out[:, 4] == 7.0) and torch.all(big_out[:, :, :8] == 7.0)
+
+
+@pytest.mark.parametrize("impl", IMPLS)
+def test_unused_pool_rows_are_never_read(impl):
+    """Every pool row no request names is NaN: any stray read poisons the output."""
+    inp = W.make_inputs([120, 64, 1], [8, 16, 3], 8, pool_size=1024, seed=22)
+    used = np.concatenate([inp.kv_indices.astype(np.int64), inp.out_cache_loc])
+    poison = np.ones(inp.pool_size, bool); poison[used] = False
+    inp.kv_pool[torch.from_numpy(poison)] = float("nan")
+    out, status = run(inp, impl=impl, num_splits=5)
+    assert status == 0
+    assert_parity(as_rows(out), oracle_rows(inp), f"poisoned pool/{impl}")
+
+
+@pytest.mark.parametrize("impl", IMPLS)
+def test_bad_slot_sets_status_without_fault(impl):
+    inp = W.make_inputs([40], [4], 2, pool_size=128, seed=23)
+    inp.kv_indices = inp.kv_indices.copy()
+    inp.kv_indices[5] = inp.pool_size + 1000
+    out, status = run(inp, impl=impl, num_splits=2)
+    assert status & api.STATUS_BAD_SLOT
+    assert np.all(np.isfinite(as_rows(out)))
+
+
+@pytest.mark.parametrize("impl", IMPLS)
+def test_too_many_drafts_sets_meta_status(impl):
+    inp = W.make_inputs([40, 12], [4, 6], 2, pool_size=128, seed=24)
+    _, status = run(inp, impl=impl, num_splits=2, max_q=5)
+    assert status & api.STATUS_BAD_META
+
+
+# ---------------------------------------------------------------- bit-exact decode
+
+@pytest.mark.parametrize("impl", IMPLS)
+def test_slot_decode_bit_exact(impl):
+    """Each pool row's V encodes its slot id in small integers (exact in bf16);
+    each draft row sees exactly one key, so the output must be that row's V
+    bit for bit.  Checks slot resolution through kv_indices / out_cache_loc."""
+    prefix, drafts, H = [700, 90, 3], [9, 5, 12], 4
+    inp = W.make_inputs(prefix, drafts, H, pool_size=4096, seed=25)
+    slots = np.arange(inp.pool_size)
+    code = np.stack([((slots >> k) & 1) * 2 - 1 + (k % 3) for k in range(12)], axis=1).astype(np.float32)
+    pool = np.zeros((inp.pool_size, 576), np.float32)
+    pool[:, :12] = code
+    pool[:, 12] = (slots % 251).astype(np.float32)
+    inp.kv_pool = torch.from_numpy(W.to_bf16_bits(pool).view(np.int16)).view(torch.bfloat16)
+    rng = np.random.default_rng(25)
+    rows_bits, picks = [], []
+    for l, t in zip(prefix, drafts):
+        n = l + t
+        pick = rng.integers(0, n, size=t)
+        m = np.zeros((t, n), bool); m[np.arange(t), pick] = True
+        rows_bits.append(m); picks.append(pick)
+    inp.custom_mask, inp.mask_indptr = W.pack_mask(rows_bits)
+    out, status = run(inp, impl=impl, num_splits=7)
+    assert status == 0
+    got = out.view(torch.int16).cpu().numpy().reshape(inp.total_q, H, 512)
+    poolbits = W.to_bf16_bits(pool)[:, :512].view(np.int16)
+    t = 0
+    for b, (l, n_t) in enumerate(zip(prefix, drafts)):
+        for i in range(n_t):
+            j = int(picks[b][i])
+            slot = inp.kv_indices[inp.kv_indptr[b] + j] if j < l else inp.out_cache_loc[inp.qo_indptr[b] + j - l]
+            for h in range(H):
+                assert np.array_equal(got[t, h], poolbits[slot]), f"request {b} draft {i} head {h}"
+            t += 1
+
+
+@pytest.mark.parametrize("impl", IMPLS)
+def test_mask_decode_bit_exact(impl):
+    """q = 0 gives every visible key equal weight; key j's V is one-hot on dim
+    j, so out[row, j] != 0 exactly when the mask lets row see key j.  The
+    recovered bit matrix must equal the packed mask bit for bit."""
+    prefix, drafts, H = [230, 41], [20, 33], 2
+    rng = np.random.default_rng(26)
+    pv = [rng.random((t, l)) < 0.7 for l, t in zip(prefix, drafts)]
+    inp = W.make_inputs(prefix, drafts, H, pool_size=1024, seed=26,
+                        extra_prefix_mask=lambda b, t, l: pv[b])
+    pool = np.zeros((inp.pool_size, 576), np.float32)
+    for b, (l, t) in enumerate(zip(prefix, drafts)):
+        for j in range(l + t):
+            slot = inp.kv_indices[inp.kv_indptr[b] + j] if j < l else inp.out_cache_loc[inp.qo_indptr[b] + j - l]
+            pool[slot, j] = 1.0
+    inp.kv_pool = torch.from_numpy(W.to_bf16_bits(pool).view(np.int16)).view(torch.bfloat16)
+    inp.q = torch.zeros_like(inp.q)
+    out, status = run(inp, impl=impl, num_splits=4)
+    assert status == 0
+    got = out.float().cpu().numpy().reshape(inp.total_q, H, 512)
+    bits = np.unpackbits(inp.custom_mask, bitorder="little")
+    t = 0
+    for b, (l, n_t) in enumerate(zip(prefix, drafts)):
+        n = l + n_t
+        for i in range(n_t):
+            want = bits[int(inp.mask_indptr[b]) + i * n: int(inp.mask_indptr[b]) + (i + 1) * n].astype(bool)
+            for h in range(H):
+                assert np.array_equal(got[t, h, :n] != 0, want), f"request {b} draft {i}"
+                assert np.all(got[t, h, n:] == 0)
+            t += 1
+
+
+# ---------------------------------------------------------------- CUDA graph capture / replay
+
+@pytest.mark.parametrize("impl", IMPLS)
+def test_graph_capture_and_replay_with_new_contents(impl):
+    """Capture one call, then rewrite the *contents* of the static buffers
+    (new trees, new slots, new prefix lengths, new q) and replay: each replay
+    must match the oracle on the new inputs ("The Capture-Safe Kernel",
+    Decision 6: no replay hook, the kernel reads the static buffers)."""
+    B, max_q, H, splits, pool_size = 3, 16, 8, 8, 8192
+    cap_kv, cap_bits = 3 * 1500, 3 * 16 * (1500 + 16)
+    pool = W.make_inputs([1], [1], H, pool_size=pool_size, seed=30).kv_pool.cuda()
+    st = {
+        "q": torch.zeros(B * max_q, H, 576, dtype=torch.bfloat16, device="cuda"),
+        "qo_indptr": torch.zeros(B + 1, dtype=torch.int32, device="cuda"),
+        "kv_indptr": torch.zeros(B + 1, dtype=torch.int32, device="cuda"),
+        "kv_indices": torch.zeros(cap_kv, dtype=torch.int32, device="cuda"),
+        "out_cache_loc": torch.zeros(B * max_q, dtype=torch.int64, device="cuda"),
+        "custom_mask": torch.zeros(cap_bits // 8 + 1, dtype=torch.uint8, device="cuda"),
+        "mask_indptr": torch.zeros(B + 1, dtype=torch.int64, device="cuda"),
+    }
+    out = torch.zeros(B * max_q, H, 512, dtype=torch.bfloat16, device="cuda")
+    runner = api.VerifyAttention(B, max_q, H, splits, impl=impl)
+
+    def fill(inp):
+        for k in ("qo_indptr", "kv_indptr", "kv_indices", "out_cache_loc", "custom_mask", "mask_indptr"):
+            src = torch.from_numpy(np.ascontiguousarray(getattr(inp, k))).cuda()
+            st[k][: src.numel()].copy_(src)
+        st["q"].zero_()
+        st["q"][: inp.total_q].copy_(inp.q.cuda())
+
+    def call():
+        runner(st["q"], pool, st["qo_indptr"], st["kv_indptr"], st["kv_indices"], st["out_cache_loc"],
+               st["custom_mask"], st["mask_indptr"], W.SM_SCALE, out)
+
+    first = W.make_inputs([1000, 10, 400], [16, 3, 9], H, pool_size=pool_size, seed=31)
+    first.kv_pool = pool.cpu()
+    fill(first)
+    call()                                   # warm-up outside capture
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(g, stream=s):
+            call()
+    torch.cuda.synchronize()
+    for seed, prefix, drafts in [(32, [1500, 700, 1], [5, 16, 2]), (33, [3, 1400, 1499], [16, 1, 16]),
+                                 (34, [0, 0, 1200], [2, 2, 2])]:
+        inp = W.make_inputs(prefix, drafts, H, pool_size=pool_size, seed=seed)
+        inp.kv_pool = pool.cpu()
+        fill(inp)
+        g.replay()
+        torch.cuda.synchronize()
+        got = as_rows(out)[: inp.total_q * H]
+        assert_parity(got, oracle_rows(inp), f"replay seed {seed}/{impl}")
