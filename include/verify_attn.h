@@ -81,6 +81,8 @@ enum verify_attn_status {
     VA_ERR_LAUNCH = -6,     /* a CUDA launch or attribute call failed               */
     VA_ERR_SCALE = -7,      /* sm_scale not finite                                   */
     VA_ERR_DEVICE = -8,     /* the current device is not sm_103 or cannot be queried */
+    VA_ERR_SCRATCH_LIMIT = -9, /* verify_attn_run_static: the capacities need more
+                                  scratch than VERIFY_ATTN_STATIC_SCRATCH_BYTES      */
 };
 
 /* Bits of the device status word (workspace byte 0). */
@@ -188,6 +190,46 @@ VERIFY_ATTN_API int verify_attn_run_profiled(int impl, void *const *events,
                                              int batch, int max_q_per_req, int num_heads, int num_splits,
                                              void *workspace, size_t workspace_bytes,
                                              verify_attn_stream_t stream);
+
+/*
+ * Largest workspace verify_attn_run_static can stand in for: 32 MiB, held in
+ * a fixed array inside the library on every GPU that loads it.
+ */
+#define VERIFY_ATTN_STATIC_SCRATCH_BYTES ((size_t)32 << 20)
+
+/*
+ * verify_attn_run without a workspace argument, for callers that cannot
+ * allocate device memory: engines that reserve almost all GPU memory for
+ * their KV pool up front and allow no later allocation, host programs that
+ * load this library as a plug-in without giving it an allocator, or paths
+ * where an allocation would synchronise the device.  (The pages have no
+ * counterpart: their workspace is always a caller tensor.)
+ *
+ * The library supplies the scratch itself, from a fixed 32 MiB device array
+ * (VERIFY_ATTN_STATIC_SCRATCH_BYTES) compiled into it.  Capacities whose
+ * verify_attn_workspace_size(...) exceeds that are rejected with
+ * VA_ERR_SCRATCH_LIMIT before anything is launched.  The call allocates
+ * nothing (no cudaMalloc, no cudaFree, no allocating library routine).
+ *
+ * The first call on each device looks up the array's device address with
+ * that device current and caches it; make that first call before any stream
+ * capture.  All calls on a device share the one array and it keeps the last
+ * call's contents; each call clears the part that must start at zero (the
+ * status word).  Calls whose GPU work overlaps -- for instance on two
+ * streams at once -- race on that array, so serialise them.  The status
+ * word lives inside the array and is not readable by the caller.
+ *
+ * Arguments, layouts and the other return codes are those of verify_attn_run.
+ */
+VERIFY_ATTN_API int verify_attn_run_static(const void *q, int64_t q_stride_tok, int64_t q_stride_head,
+                                           const void *kv_pool, int64_t pool_size,
+                                           const int32_t *qo_indptr, const int32_t *kv_indptr,
+                                           const int32_t *kv_indices, const int64_t *out_cache_loc,
+                                           const uint8_t *custom_mask, const int64_t *mask_indptr,
+                                           float sm_scale,
+                                           void *out, int64_t out_stride_tok, int64_t out_stride_head,
+                                           int batch, int max_q_per_req, int num_heads, int num_splits,
+                                           verify_attn_stream_t stream);
 
 /* Short English description of a VA_* status code (static storage). */
 VERIFY_ATTN_API const char *verify_attn_status_string(int status);

@@ -204,6 +204,7 @@ const char *verify_attn_status_string(int status)
     case VA_ERR_LAUNCH: return "CUDA launch failed";
     case VA_ERR_SCALE: return "sm_scale is not finite";
     case VA_ERR_DEVICE: return "current device is not sm_103";
+    case VA_ERR_SCRATCH_LIMIT: return "capacities need more scratch than the static 32 MiB array";
     default: return "unknown status";
     }
 }
