@@ -140,6 +140,9 @@ def verify_attn(q: torch.Tensor, kv_pool: torch.Tensor, qo_indptr: torch.Tensor,
     if impl not in ("tc", "simt"):
         raise ValueError(f"unknown impl {impl!r}")
     if events is not None:
+        for e in events:                 # torch creates the CUDA event lazily, on first record
+            if e is not None and not e.cuda_event:
+                e.record(s)
         ev = (ctypes.c_void_p * 4)(*[e.cuda_event if e is not None else 0 for e in events])
         fn = lambda *a: lib.verify_attn_run_profiled(0 if impl == "tc" else 1, ev, *a)
     else:
