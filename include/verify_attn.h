@@ -89,6 +89,8 @@ enum verify_attn_status {
 #define VA_STATUS_BAD_SLOT 0x1u   /* slot outside [0,pool_size) or null index buffer */
 #define VA_STATUS_BAD_META 0x2u   /* some T_b > max_q_per_req, or negative lengths;
                                      rows past the capacity are not computed        */
+#define VA_STATUS_TIMEOUT 0x4u    /* a bounded wait inside a kernel expired (1 s); the
+                                     output of that call is not valid               */
 
 /*
  * Workspace bytes needed by verify_attn_run / verify_attn_run_simt for a
@@ -130,8 +132,8 @@ VERIFY_ATTN_API int verify_attn_init(void);
  *   batch, max_q_per_req, num_heads, num_splits: host capacities that fix
  *                the launch grid (so one captured graph serves every batch
  *                with these bounds).  Request b's keys are cut into chunks of
- *                c_b = ceil(N_b/num_splits) rounded up to a multiple of 64;
- *                splits past the end exit at once (Decision 3).
+ *                c_b = max(ceil(N_b/num_splits), 256) rounded up to a multiple
+ *                of 64; splits past the end exit at once (Decision 3).
  *   workspace    device scratch of workspace_bytes (see above), 256-B aligned.
  *
  * The index buffers and the mask are read in place, inside the kernels; the

@@ -24,6 +24,7 @@ V_DIM = 512
 MAX_SPLITS = 256
 STATUS_BAD_SLOT = 0x1
 STATUS_BAD_META = 0x2
+STATUS_TIMEOUT = 0x4
 
 _lock = threading.Lock()
 _lib = None

@@ -11,10 +11,12 @@ namespace va {
 constexpr int D = 576;            // latent row: 512 no-PE + 64 RoPE dims
 constexpr int DV = 512;           // V = first 512 dims of the row
 constexpr int KEY_ALIGN = 64;     // split chunks are multiples of this many keys
+constexpr int MIN_CHUNK = 256;    // and at least this long (a split reloads its query tile)
 constexpr size_t WS_HEADER = 256; // status word + padding at the workspace start
 
 constexpr unsigned STATUS_BAD_SLOT = 0x1u;   // slot outside the pool / null index buffer
 constexpr unsigned STATUS_BAD_META = 0x2u;   // T_b > max_q_per_req or negative lengths
+constexpr unsigned STATUS_TIMEOUT = 0x4u;    // a bounded wait inside a kernel expired
 
 // Everything one call needs, by value (kernel parameter).
 struct Params {
@@ -39,10 +41,12 @@ struct Params {
 };
 
 // Keys per split for a request with n keys: the pages' ceil(n / NSPLIT)
-// ("The Capture-Safe Kernel", Decision 3), rounded up to a whole key tile.
+// ("The Capture-Safe Kernel", Decision 3), at least MIN_CHUNK, rounded up
+// to a whole key tile.  A request uses ceil(n / chunk) <= num_splits splits.
 __host__ __device__ inline int64_t split_chunk(int64_t n, int num_splits)
 {
     int64_t c = (n + num_splits - 1) / num_splits;
+    if (c < MIN_CHUNK) c = MIN_CHUNK;
     return (c + KEY_ALIGN - 1) / KEY_ALIGN * KEY_ALIGN;
 }
 

@@ -1,14 +1,556 @@
-// Tensor-core (tcgen05 / TMEM) split kernel for sm_103a -- placeholder until
-// the kernel lands; tc_supported() is false so verify_attn_run uses the
-// CUDA-core kernel.
+// Tensor-core split kernel for tree-verify attention (sm_103a: tcgen05, TMEM).
+//
+// Work unit: one (key split, 128-row tile, request), the same unit as the
+// pages' split-KV flash-decode partial ("The Capture-Safe Kernel",
+// Decision 3), but every key tile is loaded once per 128 rows (T*H rows of
+// one request share all keys: MLA latent attention, "The Integration
+// Chasm", section Decision) and both contractions run on the tensor cores.
+//
+// Why a 2-CTA cluster per unit.  A 128 x 512 fp32 output accumulator is the
+// whole of an SM's TMEM (128 lanes x 512 columns), and a 128 x 576 bf16 Q
+// tile is 144 KB of shared memory, so one SM cannot hold Q, the scores S
+// and O for 128 rows while feeding M = 128 MMAs at full rate.  The pair
+// splits the work by role:
+//
+//   CTA rank 0 ("S"): Q lives in TMEM (288 columns of packed bf16, the A
+//     operand of S = Q K^T from tensor memory); K tiles (64 keys x 576) are
+//     gathered into shared memory; two 64-column S buffers in TMEM.  Its
+//     four row warps (thread = row) read S, apply the packed tree mask, run
+//     the online softmax and write P (bf16) straight into the partner's
+//     shared memory.
+//   CTA rank 1 ("O"): the 128 x 512 fp32 O accumulator fills its TMEM;
+//     V tiles (64 keys x 512, the first 512 dims of the same rows) are
+//     gathered into shared memory; O += P V on the tensor cores.
+//
+// Per 64-key tile the S CTA issues 36 MMAs (M128 N64 K16, A from TMEM) and
+// the O CTA 8 (M128 N256 K16, both operands in shared memory), so the two
+// SMs carry 576 and 512 MACs per (row, key): balanced.
+//
+// Online softmax uses a lazy maximum: O is rescaled only when a row's
+// running maximum grows by more than 2^8 (log2 units), so P stays <= 256;
+// the S CTA sends the per-row factor and a per-warp flag with each P tile
+// and the O CTA's row warps rescale their TMEM rows only on flagged tiles.
+//
+// Each thread role, the barriers between them, and the shared-memory
+// layouts (128-byte swizzle; one gathered tile serves as K-major B of
+// Q K^T and as MN-major B of P V) are described where they are defined.
+// Every wait is bounded (1 s of global time): on expiry the kernel sets
+// STATUS_TIMEOUT, unwinds, drains its MMAs and frees TMEM.
 #include "va_internal.cuh"
+#include "tc_ptx.cuh"
+
+#include <math.h>
 
 namespace va {
+namespace {
 
-cudaError_t tc_init() { return cudaSuccess; }
+using namespace ptx;
 
-bool tc_supported(const Params &) { return false; }
+constexpr int ROWS = 128;                  // rows per unit = M of every MMA
+constexpr int KEYS = 64;                   // keys per tile
+constexpr int STAGES = 3;                  // gathered tiles in flight per CTA
+constexpr int THREADS = 288;               // warps 0-3 rows, 4-7 gather, 8 MMA issue
+constexpr int PRODUCER_WARP0 = 4;
+constexpr int MMA_WARP = 8;
+constexpr int PRODUCERS = 128;
+constexpr uint32_t CHUNK_BYTES = KEYS * 128;          // one 64-dim column block of a tile
+constexpr uint32_t K_CHUNKS = D / 64;                 // 9
+constexpr uint32_t V_CHUNKS = DV / 64;                // 8
+constexpr uint32_t K_STAGE = K_CHUNKS * CHUNK_BYTES;  // 73728
+constexpr uint32_t V_STAGE = V_CHUNKS * CHUNK_BYTES;  // 65536
+constexpr uint32_t P_BUF = ROWS * KEYS * 2;           // 16384
+constexpr uint32_t HEADER = 2048;
+constexpr uint32_t STAGE0 = HEADER;                   // both roles: gathered tiles
+constexpr uint32_t PBUF0 = HEADER + STAGES * V_STAGE; // O role: two P buffers
+constexpr uint32_t SMEM_USED = PBUF0 + 2 * P_BUF;
+constexpr uint32_t SMEM_ALLOC = SMEM_USED + 1024;     // room to align the base to 1 KB
+static_assert(STAGE0 + STAGES * K_STAGE <= SMEM_USED, "S role layout");
+static_assert(SMEM_ALLOC <= 232448, "at most 227 KB of shared memory per CTA");
 
-cudaError_t launch_tc_split(const Params &, cudaStream_t) { return cudaErrorNotSupported; }
+constexpr uint32_t TMEM_COLS = 512;
+constexpr uint32_t TM_Q = 0;                          // S role: 288 columns
+constexpr uint32_t TM_S0 = 320;                       // S role: S buffers at 320 and 384
+constexpr uint32_t IDESC_S = idesc_bf16(128, 64, false);
+constexpr uint32_t IDESC_PV = idesc_bf16(128, 256, true);
+constexpr float LOG2E = 1.4426950408889634f;
+constexpr float LN2 = 0.69314718055994531f;
+constexpr float RESCALE_LOG2 = 8.0f;
+constexpr uint64_t TIMEOUT_NS = 1000000000ull;
+
+// Shared-memory header at the (1 KB aligned) base; same offsets in both CTAs
+// so a barrier or field can be addressed in the partner with mapa.
+struct Header {
+    uint64_t k_full[STAGES];   // S: gathered K tile landed (128 cp.async arrivals + 4 warp leaders)
+    uint64_t k_empty[STAGES];  // S: MMAs reading the stage completed (commit)
+    uint64_t s_full[2];        // S: scores ready (commit) + valid-key bits published (MMA thread)
+    uint64_t s_free[2];        // S: 128 row threads have read the score buffer
+    uint64_t p_empty[2];       // S: partner done with a P buffer (its commit + its 4 row-warp leaders)
+    uint64_t v_full[STAGES];   // O: gathered V tile landed (128 cp.async arrivals)
+    uint64_t v_empty[STAGES];  // O: MMAs reading the stage completed
+    uint64_t p_full[2];        // O: partner's 128 row threads wrote a P tile
+    uint64_t pv_sync;          // O: every MMA issued so far completed (before a rescale)
+    uint64_t rs_req;           // O: MMA thread asks the row warps to rescale O
+    uint64_t rs_done;          // O: 128 row threads rescaled their rows
+    uint64_t l_ready;          // O: partner's 128 row threads wrote 1/l
+    uint64_t drain;            // both: all MMAs of the CTA completed
+    uint64_t k_valid[STAGES];  // S: bit n = key n of the stage has a valid slot
+    uint64_t s_valid[2];       // S: the same bits, per score buffer
+    uint32_t tmem_base;
+    uint32_t abort;
+    uint32_t flags[2];         // O: byte w != 0 if a row of warp w rescales on this P buffer
+    float alpha[2][ROWS];      // O: per-row rescale factor for the tile in each P buffer
+    float inv_l[ROWS];         // O: 1 / softmax denominator per row (0 if the row saw nothing)
+};
+static_assert(sizeof(Header) <= HEADER, "header fits");
+
+struct Unit {
+    int split, b;
+    int64_t qo0, kv0, L, N, k0, k1, r0, rows_b;
+    int ntiles;
+};
+
+// Bounded wait on phase `parity` of a barrier.  False after a timeout (status
+// bit set, abort flag raised) or when another thread of the CTA aborted.
+__device__ __noinline__ bool wait_bar(Header *h, uint32_t bar, uint32_t parity, unsigned *status, bool cluster,
+                                      bool stop_on_abort = true)
+{
+    if (cluster ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = globaltimer_ns();
+    for (uint32_t it = 1;; ++it) {
+        if (cluster ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity)) return true;
+        if ((it & 63u) == 0) {
+            if (stop_on_abort && *reinterpret_cast<volatile uint32_t *>(&h->abort)) return false;
+            if (globaltimer_ns() - t0 > TIMEOUT_NS) {
+                atomicOr(status, STATUS_TIMEOUT);
+                *reinterpret_cast<volatile uint32_t *>(&h->abort) = 1u;
+                return false;
+            }
+        }
+    }
+}
+
+// The same for all 32 lanes of a warp: true only if every lane's wait succeeded
+// (keeps the warp converged for the .sync.aligned tcgen05 instructions).
+__device__ __forceinline__ bool warp_wait(Header *h, uint32_t bar, uint32_t parity, unsigned *status, bool cluster)
+{
+    return __all_sync(0xffffffffu, wait_bar(h, bar, parity, status, cluster)) != 0;
+}
+
+// nbits (<= 64) mask bits starting at bit index bit0, bit n of the result =
+// bit bit0 + n; bytes are read only inside that range.
+__device__ __forceinline__ uint64_t load_bits(const uint8_t *mask, int64_t bit0, int nbits)
+{
+    if (nbits <= 0) return 0ull;
+    const int64_t first = bit0 >> 3, last = (bit0 + nbits - 1) >> 3;
+    const int nb = (int)(last - first + 1);
+    uint64_t lo = 0, hi = 0;
+#pragma unroll
+    for (int k = 0; k < 9; ++k) {
+        if (k < nb) {
+            const uint64_t v = __ldg(mask + first + k);
+            if (k < 8) lo |= v << (8 * k); else hi = v;
+        }
+    }
+    const int sh = (int)(bit0 & 7);
+    uint64_t w = sh ? ((lo >> sh) | (hi << (64 - sh))) : lo;
+    if (nbits < 64) w &= (1ull << nbits) - 1ull;
+    return w;
+}
+
+// ------------------------------------------------------------------ gather (warps 4-7, both roles)
+//
+// Tile layout in shared memory: NCH column blocks of 64 dims; block c holds
+// the 64 keys as 128-B rows (key n at n*128), 16-B pieces swizzled as
+// piece q -> q ^ (n & 7) inside each 1 KB group of 8 keys.  Read as B of
+// Q K^T it is K-major (rows = keys); read as B of P V it is MN-major (64
+// contiguous dims per key row, 8 keys per 1 KB group).
+template <int NCH>
+__device__ void gather_tiles(const Params &p, Header *h, uint32_t stage_base, uint32_t stage_bytes,
+                             uint64_t *full, uint64_t *empty, uint64_t *valid, const Unit &u)
+{
+    const int pw = (int)(threadIdx.x >> 5) - PRODUCER_WARP0;
+    const int lane = threadIdx.x & 31;
+    for (int t = 0; t < u.ntiles; ++t) {
+        const int stage = t % STAGES;
+        if (t >= STAGES && !wait_bar(h, smem_u32(&empty[stage]), (uint32_t)((t / STAGES) - 1) & 1u, p.status, false))
+            break;
+        const int64_t jbase = u.k0 + (int64_t)t * KEYS + pw * 16;
+        int64_t slot = -1;
+        if (lane < 16) {
+            const int64_t j = jbase + lane;
+            if (j < u.k1) slot = key_slot(p, u.kv0, u.qo0, u.L, j);
+        }
+        const uint32_t ok = __ballot_sync(0xffffffffu, lane < 16 && slot >= 0) & 0xFFFFu;
+        const uint32_t sb = stage_base + (uint32_t)stage * stage_bytes;
+#pragma unroll 1
+        for (int kk = 0; kk < 16; ++kk) {
+            const int64_t s = __shfl_sync(0xffffffffu, slot, kk);
+            const int n = pw * 16 + kk;
+            const __nv_bfloat16 *src = p.kv_pool + (s >= 0 ? s : 0) * D;
+            const uint32_t bytes = s >= 0 ? 16u : 0u;
+            const uint32_t row = sb + (uint32_t)n * 128u;
+#pragma unroll
+            for (int piece = lane; piece < NCH * 8; piece += 32) {
+                const uint32_t c = (uint32_t)piece >> 3, q = (uint32_t)piece & 7u;
+                cp_async16(row + c * CHUNK_BYTES + ((q ^ ((uint32_t)n & 7u)) << 4), src + piece * 8, bytes);
+            }
+        }
+        cp_async_arrive_noinc(smem_u32(&full[stage]));
+        if (valid != nullptr && lane == 0) {
+            reinterpret_cast<volatile uint16_t *>(&valid[stage])[pw] = (uint16_t)ok;
+            mbar_arrive(smem_u32(&full[stage]));
+        }
+    }
+    cp_async_wait_all();
+}
+
+// ------------------------------------------------------------------ S role
+
+// MMA issue (warp 8, lane 0): S[buf] = Q K^T for every tile.
+__device__ void s_role_mma(const Params &p, Header *h, uint32_t smem, uint32_t tmem, const Unit &u)
+{
+    for (int t = 0; t < u.ntiles; ++t) {
+        const int stage = t % STAGES, buf = t & 1;
+        if (!wait_bar(h, smem_u32(&h->k_full[stage]), (uint32_t)(t / STAGES) & 1u, p.status, false)) break;
+        if (t >= 2 && !wait_bar(h, smem_u32(&h->s_free[buf]), (uint32_t)((t >> 1) - 1) & 1u, p.status, false))
+            break;
+        tc_fence_after_sync();
+        fence_proxy_async_smem();
+        *reinterpret_cast<volatile uint64_t *>(&h->s_valid[buf]) =
+            *reinterpret_cast<volatile uint64_t *>(&h->k_valid[stage]);
+        const uint32_t kb = smem + STAGE0 + (uint32_t)stage * K_STAGE;
+        const uint32_t d = tmem + TM_S0 + 64u * (uint32_t)buf;
+#pragma unroll 4
+        for (int k = 0; k < D / 16; ++k) {
+            const uint64_t bdesc = sdesc_sw128(kb + (uint32_t)(k >> 2) * CHUNK_BYTES + (uint32_t)(k & 3) * 32u, 16u, 1024u);
+            mma_ts(d, tmem + TM_Q + 8u * (uint32_t)k, bdesc, IDESC_S, k > 0 ? 1u : 0u);
+        }
+        mma_commit(smem_u32(&h->k_empty[stage]));
+        mma_commit(smem_u32(&h->s_full[buf]));
+        mbar_arrive(smem_u32(&h->s_full[buf]));
+    }
+    mma_commit(smem_u32(&h->drain));
+    wait_bar(h, smem_u32(&h->drain), 0u, p.status, false, false);
+}
+
+// Row warps (thread = row): Q into TMEM, then per tile mask + online softmax
+// + P to the partner; finally lse to the workspace and 1/l to the partner.
+__device__ void s_role_rows(const Params &p, Header *h, uint32_t smem, uint32_t tmem, const Unit &u)
+{
+    const int r = threadIdx.x, warp = r >> 5, lane = r & 31;
+    const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+    const int H = p.num_heads;
+    const int64_t lr = u.r0 + r;
+    const bool row_ok = lr < u.rows_b;
+    const int64_t i = row_ok ? lr / H : 0;
+    const int64_t hh = row_ok ? lr % H : 0;
+
+    // Q row -> TMEM columns [0, 288): 32-bit column k/2 holds elements k, k+1.
+    const __nv_bfloat16 *qrow = p.q + (u.qo0 + i) * p.q_stride_tok + hh * p.q_stride_head;
+#pragma unroll 1
+    for (int c = 0; c < D / 64; ++c) {
+        uint32_t w[32];
+#pragma unroll
+        for (int v = 0; v < 8; ++v) {
+            uint4 x = make_uint4(0u, 0u, 0u, 0u);
+            if (row_ok) x = __ldg(reinterpret_cast<const uint4 *>(qrow + c * 64 + v * 8));
+            w[4 * v] = x.x; w[4 * v + 1] = x.y; w[4 * v + 2] = x.z; w[4 * v + 3] = x.w;
+        }
+        tmem_st32(tmem + lane_base + TM_Q + 32u * (uint32_t)c, w);
+    }
+    tmem_st_wait();
+    tc_fence_before_sync();
+    named_barrier_sync(1, 160);
+
+    const int64_t mrow = p.mask_indptr[u.b] + i * u.N;
+    const float sl2 = p.sm_scale * LOG2E;
+    const uint32_t peer_pbuf = map_cluster(smem + PBUF0, 1);
+    const uint32_t peer_alpha = map_cluster(smem_u32(&h->alpha[0][0]), 1);
+    const uint32_t peer_flags = map_cluster(smem_u32(&h->flags[0]), 1);
+    float m_used = -INFINITY, l = 0.f;
+    bool ok = true;
+
+    for (int t = 0; t < u.ntiles; ++t) {
+        const int buf = t & 1;
+        const int64_t j0 = u.k0 + (int64_t)t * KEYS;
+        if (!warp_wait(h, smem_u32(&h->s_full[buf]), (uint32_t)(t >> 1) & 1u, p.status, false)) { ok = false; break; }
+        tc_fence_after_sync();
+        uint32_t sa[32], sb[32];
+        tmem_ld32(tmem + lane_base + TM_S0 + 64u * (uint32_t)buf, sa);
+        tmem_ld32(tmem + lane_base + TM_S0 + 64u * (uint32_t)buf + 32u, sb);
+        tmem_ld_wait();
+        tc_fence_before_sync();
+        mbar_arrive(smem_u32(&h->s_free[buf]));
+
+        const uint64_t valid = *reinterpret_cast<volatile uint64_t *>(&h->s_valid[buf]);
+        const int nk = (int)((u.k1 - j0) < KEYS ? (u.k1 - j0) : KEYS);
+        const uint64_t vis = valid & (row_ok ? load_bits(p.custom_mask, mrow + j0, nk) : 0ull);
+
+        float mx = -INFINITY;
+#pragma unroll
+        for (int n = 0; n < 32; ++n) {
+            const float s0 = ((vis >> n) & 1ull) ? __uint_as_float(sa[n]) * sl2 : -INFINITY;
+            const float s1 = ((vis >> (n + 32)) & 1ull) ? __uint_as_float(sb[n]) * sl2 : -INFINITY;
+            sa[n] = __float_as_uint(s0);
+            sb[n] = __float_as_uint(s1);
+            mx = fmaxf(mx, fmaxf(s0, s1));
+        }
+        float alpha = 1.f;
+        bool rescale = false;
+        if (mx > m_used + RESCALE_LOG2) {        // also the first tile where the row sees a key
+            alpha = (m_used == -INFINITY) ? 0.f : ex2_approx(m_used - mx);
+            l *= alpha;
+            m_used = mx;
+            rescale = true;
+        }
+        if (t >= 2 && !warp_wait(h, smem_u32(&h->p_empty[buf]), (uint32_t)((t >> 1) - 1) & 1u, p.status, true)) {
+            ok = false;
+            break;
+        }
+        uint32_t pk[32];
+        float psum = 0.f;
+#pragma unroll
+        for (int n = 0; n < 16; ++n) {
+            const float a0 = __uint_as_float(sa[2 * n]), a1 = __uint_as_float(sa[2 * n + 1]);
+            const float b0 = __uint_as_float(sb[2 * n]), b1 = __uint_as_float(sb[2 * n + 1]);
+            const float pa0 = a0 == -INFINITY ? 0.f : ex2_approx(a0 - m_used);
+            const float pa1 = a1 == -INFINITY ? 0.f : ex2_approx(a1 - m_used);
+            const float pb0 = b0 == -INFINITY ? 0.f : ex2_approx(b0 - m_used);
+            const float pb1 = b1 == -INFINITY ? 0.f : ex2_approx(b1 - m_used);
+            psum += (pa0 + pa1) + (pb0 + pb1);
+            pk[n] = pack_bf16x2(pa0, pa1);
+            pk[16 + n] = pack_bf16x2(pb0, pb1);
+        }
+        l += psum;
+        // Row r of the partner's P buffer: K-major, 128-B swizzle (A of P V).
+        const uint32_t prow = peer_pbuf + (uint32_t)buf * P_BUF + (uint32_t)(r >> 3) * 1024u + (uint32_t)(r & 7) * 128u;
+#pragma unroll
+        for (int q = 0; q < 8; ++q)
+            st_cluster_v4(prow + (((uint32_t)q ^ (uint32_t)(r & 7)) << 4), pk[4 * q], pk[4 * q + 1], pk[4 * q + 2],
+                          pk[4 * q + 3]);
+        st_cluster_f32(peer_alpha + (uint32_t)(buf * ROWS + r) * 4u, rescale ? alpha : 1.f);
+        const uint32_t any = __any_sync(0xffffffffu, rescale) ? 1u : 0u;
+        if (lane == 0) st_cluster_u8(peer_flags + (uint32_t)buf * 4u + (uint32_t)warp, any);
+        fence_proxy_async_all();
+        mbar_arrive_cluster(smem_u32(&h->p_full[buf]), 1);
+    }
+
+    if (ok && row_ok) {
+        const int64_t row = u.qo0 * H + lr;
+        if (row < p.rows_cap)
+            p.part_lse[(int64_t)u.split * p.rows_cap + row] = l > 0.f ? (m_used + log2f(l)) * LN2 : -INFINITY;
+    }
+    st_cluster_f32(map_cluster(smem_u32(&h->inv_l[r]), 1), l > 0.f ? 1.f / l : 0.f);
+    mbar_arrive_cluster(smem_u32(&h->l_ready), 1);
+}
+
+// ------------------------------------------------------------------ O role
+
+// MMA issue (warp 8, lane 0): O += P V for every tile, both 256-column halves.
+__device__ void o_role_mma(const Params &p, Header *h, uint32_t smem, uint32_t tmem, const Unit &u)
+{
+    uint32_t nrs = 0;
+    for (int t = 0; t < u.ntiles; ++t) {
+        const int stage = t % STAGES, buf = t & 1;
+        if (!wait_bar(h, smem_u32(&h->v_full[stage]), (uint32_t)(t / STAGES) & 1u, p.status, false)) break;
+        if (!wait_bar(h, smem_u32(&h->p_full[buf]), (uint32_t)(t >> 1) & 1u, p.status, true)) break;
+        const uint32_t flags = t > 0 ? *reinterpret_cast<volatile uint32_t *>(&h->flags[buf]) : 0u;
+        if (flags) {
+            mma_commit(smem_u32(&h->pv_sync));
+            if (!wait_bar(h, smem_u32(&h->pv_sync), nrs & 1u, p.status, false)) break;
+            mbar_arrive(smem_u32(&h->rs_req));
+            if (!wait_bar(h, smem_u32(&h->rs_done), nrs & 1u, p.status, false)) break;
+            ++nrs;
+        }
+        tc_fence_after_sync();
+        fence_proxy_async_smem();
+        const uint32_t pb = smem + PBUF0 + (uint32_t)buf * P_BUF;
+        const uint32_t vb = smem + STAGE0 + (uint32_t)stage * V_STAGE;
+#pragma unroll
+        for (int k = 0; k < KEYS / 16; ++k) {
+            const uint64_t adesc = sdesc_sw128(pb + 32u * (uint32_t)k, 16u, 1024u);
+#pragma unroll
+            for (int half = 0; half < 2; ++half) {
+                const uint64_t bdesc =
+                    sdesc_sw128(vb + (uint32_t)half * 4u * CHUNK_BYTES + (uint32_t)k * 16u * 128u, CHUNK_BYTES, 1024u);
+                mma_ss(tmem + 256u * (uint32_t)half, adesc, bdesc, IDESC_PV, (t > 0 || k > 0) ? 1u : 0u);
+            }
+        }
+        mma_commit(smem_u32(&h->v_empty[stage]));
+        mma_commit_multicast(smem_u32(&h->p_empty[buf]), (uint16_t)0x1);
+    }
+    mma_commit(smem_u32(&h->drain));
+}
+
+// Row warps (thread = TMEM lane = row): rescale O rows on flagged tiles;
+// after the last tile, O / l -> fp32 partial in the workspace.
+__device__ void o_role_rows(const Params &p, Header *h, uint32_t smem, uint32_t tmem, const Unit &u)
+{
+    const int r = threadIdx.x, warp = r >> 5, lane = r & 31;
+    const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+    uint32_t nrs = 0;
+    bool ok = true;
+    for (int t = 0; t < u.ntiles; ++t) {
+        const int buf = t & 1;
+        if (!warp_wait(h, smem_u32(&h->p_full[buf]), (uint32_t)(t >> 1) & 1u, p.status, true)) { ok = false; break; }
+        const uint32_t flags = t > 0 ? *reinterpret_cast<volatile uint32_t *>(&h->flags[buf]) : 0u;
+        if (flags) {
+            const float a = h->alpha[buf][r];
+            if (!warp_wait(h, smem_u32(&h->rs_req), nrs & 1u, p.status, false)) { ok = false; break; }
+            tc_fence_after_sync();
+#pragma unroll 1
+            for (int c = 0; c < DV / 32; ++c) {
+                uint32_t v[32];
+                tmem_ld32(tmem + lane_base + 32u * (uint32_t)c, v);
+                tmem_ld_wait();
+#pragma unroll
+                for (int e = 0; e < 32; ++e) v[e] = __float_as_uint(__uint_as_float(v[e]) * a);
+                tmem_st32(tmem + lane_base + 32u * (uint32_t)c, v);
+            }
+            tmem_st_wait();
+            tc_fence_before_sync();
+            mbar_arrive(smem_u32(&h->rs_done));
+            ++nrs;
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive_cluster(smem_u32(&h->p_empty[buf]), 0);
+    }
+    if (!__all_sync(0xffffffffu, wait_bar(h, smem_u32(&h->drain), 0u, p.status, false, false))) ok = false;
+    if (!warp_wait(h, smem_u32(&h->l_ready), 0u, p.status, true)) ok = false;
+    tc_fence_after_sync();
+    const float il = h->inv_l[r];
+    const int64_t lr = u.r0 + r;
+    const int64_t row = u.qo0 * p.num_heads + lr;
+    const bool write = ok && lr < u.rows_b && row < p.rows_cap;
+    float *dst = p.part_o + ((int64_t)u.split * p.rows_cap + (write ? row : 0)) * DV;
+#pragma unroll 1
+    for (int c = 0; c < DV / 32; ++c) {
+        uint32_t v[32];
+        tmem_ld32(tmem + lane_base + 32u * (uint32_t)c, v);
+        tmem_ld_wait();
+        if (write) {
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                float4 o;
+                o.x = __uint_as_float(v[4 * e]) * il;
+                o.y = __uint_as_float(v[4 * e + 1]) * il;
+                o.z = __uint_as_float(v[4 * e + 2]) * il;
+                o.w = __uint_as_float(v[4 * e + 3]) * il;
+                *reinterpret_cast<float4 *>(dst + c * 32 + 4 * e) = o;
+            }
+        }
+    }
+}
+
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1) tc_split_kernel(Params p)
+{
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    const uint32_t smem = (raw + 1023u) & ~1023u;
+    Header *h = reinterpret_cast<Header *>(smem_raw + (smem - raw));
+    const uint32_t role = cluster_rank();
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+
+    // a1: segment decode.  Both CTAs of the pair compute the same unit, so
+    // they leave together when it is empty.
+    Unit u;
+    u.split = (int)(blockIdx.x >> 1);
+    u.b = (int)blockIdx.z;
+    u.qo0 = p.qo_indptr[u.b];
+    const int64_t T = p.qo_indptr[u.b + 1] - u.qo0;
+    u.kv0 = p.kv_indptr[u.b];
+    u.L = p.kv_indptr[u.b + 1] - u.kv0;
+    if (T < 0 || u.L < 0 || T > p.max_q_per_req) {
+        if (role == 0 && u.split == 0 && blockIdx.y == 0 && tid == 0) atomicOr(p.status, STATUS_BAD_META);
+        if (T < 0 || u.L < 0) return;
+    }
+    u.rows_b = (T < p.max_q_per_req ? T : p.max_q_per_req) * p.num_heads;
+    u.r0 = (int64_t)blockIdx.y * ROWS;
+    if (u.r0 >= u.rows_b) return;
+    u.N = u.L + T;
+    const int64_t chunk = split_chunk(u.N, p.num_splits);
+    u.k0 = (int64_t)u.split * chunk;
+    if (u.k0 >= u.N) return;
+    u.k1 = (u.k0 + chunk < u.N) ? u.k0 + chunk : u.N;
+    u.ntiles = (int)((u.k1 - u.k0 + KEYS - 1) / KEYS);
+
+    if (tid == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(smem_u32(&h->k_full[s]), PRODUCERS + 4);
+            mbar_init(smem_u32(&h->k_empty[s]), 1);
+            mbar_init(smem_u32(&h->v_full[s]), PRODUCERS);
+            mbar_init(smem_u32(&h->v_empty[s]), 1);
+        }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(smem_u32(&h->s_full[i]), 2);
+            mbar_init(smem_u32(&h->s_free[i]), ROWS);
+            mbar_init(smem_u32(&h->p_empty[i]), 1 + 4);
+            mbar_init(smem_u32(&h->p_full[i]), ROWS);
+            h->flags[i] = 0u;
+        }
+        mbar_init(smem_u32(&h->pv_sync), 1);
+        mbar_init(smem_u32(&h->rs_req), 1);
+        mbar_init(smem_u32(&h->rs_done), ROWS);
+        mbar_init(smem_u32(&h->l_ready), ROWS);
+        mbar_init(smem_u32(&h->drain), 1);
+        h->abort = 0u;
+        fence_mbar_init_cluster();
+    }
+    if (warp == MMA_WARP) {
+        tmem_alloc(smem_u32(&h->tmem_base), TMEM_COLS);
+        tmem_relinquish();
+        tc_fence_before_sync();
+    }
+    __syncthreads();
+    cluster_sync();
+    tc_fence_after_sync();
+    const uint32_t tmem = *reinterpret_cast<volatile uint32_t *>(&h->tmem_base);
+
+    if (role == 0) {
+        if (warp < 4) {
+            s_role_rows(p, h, smem, tmem, u);
+        } else if (warp < MMA_WARP) {
+            gather_tiles<K_CHUNKS>(p, h, smem + STAGE0, K_STAGE, h->k_full, h->k_empty, h->k_valid, u);
+        } else {
+            named_barrier_sync(1, 160);
+            tc_fence_after_sync();
+            if (lane == 0) s_role_mma(p, h, smem, tmem, u);
+        }
+    } else {
+        if (warp < 4) {
+            o_role_rows(p, h, smem, tmem, u);
+        } else if (warp < MMA_WARP) {
+            gather_tiles<V_CHUNKS>(p, h, smem + STAGE0, V_STAGE, h->v_full, h->v_empty, nullptr, u);
+        } else if (lane == 0) {
+            o_role_mma(p, h, smem, tmem, u);
+        }
+    }
+
+    tc_fence_before_sync();
+    __syncthreads();
+    cluster_sync();
+    if (warp == MMA_WARP) {
+        __syncwarp();
+        tc_fence_after_sync();
+        tmem_dealloc(tmem, TMEM_COLS);
+    }
+}
+
+}  // namespace
+
+cudaError_t tc_init()
+{
+    return cudaFuncSetAttribute(tc_split_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_ALLOC);
+}
+
+bool tc_supported(const Params &) { return true; }
+
+cudaError_t launch_tc_split(const Params &p, cudaStream_t stream)
+{
+    const int row_tiles = (int)((p.max_q_per_req * (int64_t)p.num_heads + ROWS - 1) / ROWS);
+    dim3 grid(2u * (unsigned)p.num_splits, (unsigned)row_tiles, (unsigned)p.batch);
+    tc_split_kernel<<<grid, THREADS, SMEM_ALLOC, stream>>>(p);
+    return cudaGetLastError();
+}
 
 }  // namespace va
