@@ -70,10 +70,9 @@ def load_peaks():
 
 
 def default_splits(cfg_name, inp, kernel):
-    """Split count that fills 152 SMs for this workload's grid."""
+    """Split count planned from this workload's lengths (host-side simulation of the grid)."""
     from speculative_decode_mla_paged_gb300 import tuning
-    return tuning.default_num_splits(inp.batch, inp.max_q_per_req, inp.num_heads,
-                                     int(max(inp.prefix_lens + inp.draft_lens)), kernel)
+    return tuning.plan_num_splits(inp.prefix_lens, inp.draft_lens, inp.num_heads, kernel)
 
 
 def kernel_hash(kernel):

@@ -106,9 +106,11 @@ __device__ __forceinline__ void fence_proxy_async_smem()
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
-__device__ __forceinline__ void fence_proxy_async_all()
+// Orders this thread's generic-proxy accesses to (any CTA's) shared memory
+// before later async-proxy accesses.
+__device__ __forceinline__ void fence_proxy_async_cluster()
 {
-    asm volatile("fence.proxy.async;" ::: "memory");
+    asm volatile("fence.proxy.async.shared::cluster;" ::: "memory");
 }
 
 // ------------------------------------------------------------------ distributed shared memory stores

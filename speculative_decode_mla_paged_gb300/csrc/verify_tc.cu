@@ -87,11 +87,11 @@ struct Header {
     uint64_t p_empty[2];       // S: partner done with a P buffer (its commit + its 4 row-warp leaders)
     uint64_t v_full[STAGES];   // O: gathered V tile landed (128 cp.async arrivals)
     uint64_t v_empty[STAGES];  // O: MMAs reading the stage completed
-    uint64_t p_full[2];        // O: partner's 128 row threads wrote a P tile
+    uint64_t p_full[2];        // O: partner's 4 row warps wrote a P tile (one arrive per warp)
     uint64_t pv_sync;          // O: every MMA issued so far completed (before a rescale)
     uint64_t rs_req;           // O: MMA thread asks the row warps to rescale O
     uint64_t rs_done;          // O: 128 row threads rescaled their rows
-    uint64_t l_ready;          // O: partner's 128 row threads wrote 1/l
+    uint64_t l_ready;          // O: partner's 4 row warps wrote 1/l
     uint64_t drain;            // both: all MMAs of the CTA completed
     uint64_t k_valid[STAGES];  // S: bit n = key n of the stage has a valid slot
     uint64_t s_valid[2];       // S: the same bits, per score buffer
@@ -170,16 +170,19 @@ __device__ void gather_tiles(const Params &p, Header *h, uint32_t stage_base, ui
 {
     const int pw = (int)(threadIdx.x >> 5) - PRODUCER_WARP0;
     const int lane = threadIdx.x & 31;
+    // Slot of key (pw*16 + lane) of tile t, or -1; resolved one tile ahead so
+    // the index load overlaps the wait for a free stage.
+    auto slot_of = [&](int t) -> int64_t {
+        const int64_t j = u.k0 + (int64_t)t * KEYS + pw * 16 + lane;
+        return (lane < 16 && t < u.ntiles && j < u.k1) ? key_slot(p, u.kv0, u.qo0, u.L, j) : -1;
+    };
+    int64_t next_slot = slot_of(0);
     for (int t = 0; t < u.ntiles; ++t) {
         const int stage = t % STAGES;
+        const int64_t slot = next_slot;
+        next_slot = slot_of(t + 1);
         if (t >= STAGES && !wait_bar(h, smem_u32(&empty[stage]), (uint32_t)((t / STAGES) - 1) & 1u, p.status, false))
             break;
-        const int64_t jbase = u.k0 + (int64_t)t * KEYS + pw * 16;
-        int64_t slot = -1;
-        if (lane < 16) {
-            const int64_t j = jbase + lane;
-            if (j < u.k1) slot = key_slot(p, u.kv0, u.qo0, u.L, j);
-        }
         const uint32_t ok = __ballot_sync(0xffffffffu, lane < 16 && slot >= 0) & 0xFFFFu;
         const uint32_t sb = stage_base + (uint32_t)stage * stage_bytes;
 #pragma unroll 1
@@ -269,10 +272,18 @@ __device__ void s_role_rows(const Params &p, Header *h, uint32_t smem, uint32_t 
     const uint32_t peer_flags = map_cluster(smem_u32(&h->flags[0]), 1);
     float m_used = -INFINITY, l = 0.f;
     bool ok = true;
+    // Mask bits of tile t for this row, loaded one tile ahead.
+    auto mask_of = [&](int t) -> uint64_t {
+        const int64_t j0 = u.k0 + (int64_t)t * KEYS;
+        const int nk = (int)((u.k1 - j0) < KEYS ? (u.k1 - j0) : KEYS);
+        return (row_ok && t < u.ntiles) ? load_bits(p.custom_mask, mrow + j0, nk) : 0ull;
+    };
+    uint64_t next_bits = mask_of(0);
 
     for (int t = 0; t < u.ntiles; ++t) {
         const int buf = t & 1;
-        const int64_t j0 = u.k0 + (int64_t)t * KEYS;
+        const uint64_t bits = next_bits;
+        next_bits = mask_of(t + 1);
         if (!warp_wait(h, smem_u32(&h->s_full[buf]), (uint32_t)(t >> 1) & 1u, p.status, false)) { ok = false; break; }
         tc_fence_after_sync();
         uint32_t sa[32], sb[32];
@@ -282,9 +293,7 @@ __device__ void s_role_rows(const Params &p, Header *h, uint32_t smem, uint32_t 
         tc_fence_before_sync();
         mbar_arrive(smem_u32(&h->s_free[buf]));
 
-        const uint64_t valid = *reinterpret_cast<volatile uint64_t *>(&h->s_valid[buf]);
-        const int nk = (int)((u.k1 - j0) < KEYS ? (u.k1 - j0) : KEYS);
-        const uint64_t vis = valid & (row_ok ? load_bits(p.custom_mask, mrow + j0, nk) : 0ull);
+        const uint64_t vis = *reinterpret_cast<volatile uint64_t *>(&h->s_valid[buf]) & bits;
 
         float mx = -INFINITY;
 #pragma unroll
@@ -331,8 +340,9 @@ __device__ void s_role_rows(const Params &p, Header *h, uint32_t smem, uint32_t 
         st_cluster_f32(peer_alpha + (uint32_t)(buf * ROWS + r) * 4u, rescale ? alpha : 1.f);
         const uint32_t any = __any_sync(0xffffffffu, rescale) ? 1u : 0u;
         if (lane == 0) st_cluster_u8(peer_flags + (uint32_t)buf * 4u + (uint32_t)warp, any);
-        fence_proxy_async_all();
-        mbar_arrive_cluster(smem_u32(&h->p_full[buf]), 1);
+        fence_proxy_async_cluster();
+        __syncwarp();
+        if (lane == 0) mbar_arrive_cluster(smem_u32(&h->p_full[buf]), 1);
     }
 
     if (ok && row_ok) {
@@ -341,7 +351,8 @@ __device__ void s_role_rows(const Params &p, Header *h, uint32_t smem, uint32_t 
             p.part_lse[(int64_t)u.split * p.rows_cap + row] = l > 0.f ? (m_used + log2f(l)) * LN2 : -INFINITY;
     }
     st_cluster_f32(map_cluster(smem_u32(&h->inv_l[r]), 1), l > 0.f ? 1.f / l : 0.f);
-    mbar_arrive_cluster(smem_u32(&h->l_ready), 1);
+    __syncwarp();
+    if (lane == 0) mbar_arrive_cluster(smem_u32(&h->l_ready), 1);
 }
 
 // ------------------------------------------------------------------ O role
@@ -453,19 +464,22 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1) tc_split
 
     // a1: segment decode.  Both CTAs of the pair compute the same unit, so
     // they leave together when it is empty.
+    // Grid: x = 2 * row tile + rank in the pair, y = split, z = request.  Row
+    // tiles vary fastest, so pairs that read the same key chunk run together
+    // and share it through L2.
     Unit u;
-    u.split = (int)(blockIdx.x >> 1);
+    u.split = (int)blockIdx.y;
     u.b = (int)blockIdx.z;
     u.qo0 = p.qo_indptr[u.b];
     const int64_t T = p.qo_indptr[u.b + 1] - u.qo0;
     u.kv0 = p.kv_indptr[u.b];
     u.L = p.kv_indptr[u.b + 1] - u.kv0;
     if (T < 0 || u.L < 0 || T > p.max_q_per_req) {
-        if (role == 0 && u.split == 0 && blockIdx.y == 0 && tid == 0) atomicOr(p.status, STATUS_BAD_META);
+        if (role == 0 && u.split == 0 && blockIdx.x == 0 && tid == 0) atomicOr(p.status, STATUS_BAD_META);
         if (T < 0 || u.L < 0) return;
     }
     u.rows_b = (T < p.max_q_per_req ? T : p.max_q_per_req) * p.num_heads;
-    u.r0 = (int64_t)blockIdx.y * ROWS;
+    u.r0 = (int64_t)(blockIdx.x >> 1) * ROWS;
     if (u.r0 >= u.rows_b) return;
     u.N = u.L + T;
     const int64_t chunk = split_chunk(u.N, p.num_splits);
@@ -485,13 +499,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1) tc_split
             mbar_init(smem_u32(&h->s_full[i]), 2);
             mbar_init(smem_u32(&h->s_free[i]), ROWS);
             mbar_init(smem_u32(&h->p_empty[i]), 1 + 4);
-            mbar_init(smem_u32(&h->p_full[i]), ROWS);
+            mbar_init(smem_u32(&h->p_full[i]), 4);
             h->flags[i] = 0u;
         }
         mbar_init(smem_u32(&h->pv_sync), 1);
         mbar_init(smem_u32(&h->rs_req), 1);
         mbar_init(smem_u32(&h->rs_done), ROWS);
-        mbar_init(smem_u32(&h->l_ready), ROWS);
+        mbar_init(smem_u32(&h->l_ready), 4);
         mbar_init(smem_u32(&h->drain), 1);
         h->abort = 0u;
         fence_mbar_init_cluster();
@@ -548,7 +562,7 @@ bool tc_supported(const Params &) { return true; }
 cudaError_t launch_tc_split(const Params &p, cudaStream_t stream)
 {
     const int row_tiles = (int)((p.max_q_per_req * (int64_t)p.num_heads + ROWS - 1) / ROWS);
-    dim3 grid(2u * (unsigned)p.num_splits, (unsigned)row_tiles, (unsigned)p.batch);
+    dim3 grid(2u * (unsigned)row_tiles, (unsigned)p.num_splits, (unsigned)p.batch);
     tc_split_kernel<<<grid, THREADS, SMEM_ALLOC, stream>>>(p);
     return cudaGetLastError();
 }

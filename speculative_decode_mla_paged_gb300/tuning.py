@@ -1,20 +1,87 @@
-"""Launch-shape defaults (host-side arithmetic only)."""
+"""Launch-shape planning (host-side arithmetic only; no attention math).
+
+The split kernels run a static grid of units (key split x row tile x
+request); ``num_splits`` is a host capacity that fixes it ("The Capture-Safe
+Kernel", Decision 3).  These helpers pick it for a known workload by
+simulating how the units fill the GPU.
+"""
 from __future__ import annotations
 
+import heapq
 import math
+from typing import Sequence
 
-NUM_SMS = 152          # GB300: 2 dies x 76 SMs
+NUM_SMS = 152                  # GB300: 2 dies x 76 SMs
+KEY_ALIGN = 64                 # must match the library's split chunk rule
+MIN_CHUNK = 256
+CANDIDATES = (1, 2, 3, 4, 5, 6, 7, 8, 10, 12, 14, 16, 20, 24, 28, 32, 40, 48, 56, 64, 80, 96, 128, 160, 192, 256)
+
+
+def split_chunk(n: int, num_splits: int) -> int:
+    """Keys per split: max(ceil(n / S), 256) rounded up to 64 (the library's rule)."""
+    c = max(-(-n // num_splits), MIN_CHUNK)
+    return -(-c // KEY_ALIGN) * KEY_ALIGN
+
+
+def splits_used(n: int, num_splits: int) -> int:
+    return 0 if n <= 0 else -(-n // split_chunk(n, num_splits))
+
+
+def simulate(prefix_lens: Sequence[int], draft_lens: Sequence[int], num_heads: int, num_splits: int,
+             kernel: str = "tc") -> float:
+    """Estimated time of one call in units of one 64-key tile of a 128-row unit.
+
+    Units are dispatched in grid order (row tile fastest, then split, then
+    request) onto the concurrent slots (76 CTA pairs for the tensor-core
+    kernel, 304 CTAs for the CUDA-core one); each costs its key tiles plus a
+    fixed start-up (query tile load, pipeline fill, partial write).  The
+    combine's workspace traffic is added on top.
+    """
+    if kernel == "simt":
+        rows, slots, overhead, tile_keys, tile_cost = 16, 2 * NUM_SMS, 2.0, 32, 1.0
+    else:
+        rows, slots, overhead, tile_keys, tile_cost = 128, NUM_SMS // 2, 8.0, 64, 1.0
+    max_q = max(draft_lens) if len(draft_lens) else 0
+    max_tiles = math.ceil(max_q * num_heads / rows)
+    free = [0.0] * slots
+    heapq.heapify(free)
+    finish = 0.0
+    total_rows_splits = 0
+    for l, t in zip(prefix_lens, draft_lens):
+        n = int(l) + int(t)
+        r_tiles = math.ceil(int(t) * num_heads / rows)
+        used = splits_used(n, num_splits)
+        chunk = split_chunk(n, num_splits) if n > 0 else 0
+        total_rows_splits += int(t) * num_heads * used
+        for s in range(num_splits):
+            keys = max(0, min(n, (s + 1) * chunk) - s * chunk) if s < used else 0
+            for rt in range(max_tiles):
+                cost = (overhead + tile_cost * math.ceil(keys / tile_keys)) if (rt < r_tiles and keys) else 0.05
+                t0 = heapq.heappop(free)
+                heapq.heappush(free, t0 + cost)
+                finish = max(finish, t0 + cost)
+    # combine: each used split's fp32 partial row (2 KB) written then read at ~6.8 TB/s,
+    # against ~0.56 us per tile unit
+    combine = total_rows_splits * 2048 * 2 / 6.8e12 / 0.56e-6
+    return finish + combine
+
+
+def plan_num_splits(prefix_lens: Sequence[int], draft_lens: Sequence[int], num_heads: int,
+                    kernel: str = "tc") -> int:
+    """The candidate split count with the smallest simulated time."""
+    n_max = max(int(l) + int(t) for l, t in zip(prefix_lens, draft_lens))
+    best, best_s = None, 1
+    for s in CANDIDATES:
+        if s > 1 and split_chunk(n_max, s) == split_chunk(n_max, s - 1) and s > n_max // MIN_CHUNK + 1:
+            break
+        cost = simulate(prefix_lens, draft_lens, num_heads, s, kernel)
+        if best is None or cost < best * 0.98:
+            best, best_s = cost, s
+    return best_s
 
 
 def default_num_splits(batch: int, max_q_per_req: int, num_heads: int, max_keys: int,
                        kernel: str = "tc") -> int:
-    """Split count so the static grid covers about two waves of the 152 SMs.
-
-    The grid is num_splits x row_tiles x batch; each split of a request needs
-    enough keys (>= 256) to amortise loading its query tile.
-    """
-    rows_per_cta, ctas_per_sm = (16, 2) if kernel == "simt" else (128, 1)
-    row_tiles = max(1, math.ceil(max_q_per_req * num_heads / rows_per_cta)) * max(1, batch)
-    splits = math.ceil(2 * NUM_SMS * ctas_per_sm / row_tiles)
-    splits = min(splits, max(1, max_keys // 256), 256)
-    return max(1, splits)
+    """Split count for a uniform batch of `batch` requests of max_keys keys each."""
+    return plan_num_splits([max_keys - max_q_per_req] * max(1, batch), [max_q_per_req] * max(1, batch),
+                           num_heads, kernel)
