@@ -1,5 +1,5 @@
 // Thin inline-PTX wrappers for sm_103a: mbarriers, cluster addressing,
-// cp.async gathers, tcgen05 (TMEM allocation, MMA, commit, TMEM loads and
+// cp.async and TMA gathers, tcgen05 (TMEM allocation, MMA, commit, TMEM loads and
 // stores) and shared-memory matrix descriptors.  Written from the PTX ISA
 // descriptions of these instructions.
 #pragma once
@@ -149,6 +149,32 @@ __device__ __forceinline__ void cp_async_arrive_noinc(uint32_t bar)
 __device__ __forceinline__ void cp_async_wait_all()
 {
     asm volatile("cp.async.wait_all;" ::: "memory");
+}
+
+// ------------------------------------------------------------------ TMA
+
+// Arrive on the barrier and add `bytes` to the transaction count its phase waits for.
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes)
+{
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+}
+
+// Four rows (y0..y3) x one box of columns starting at x of a 2-D tensor map
+// into four consecutive box-sized rows of shared memory at dst (swizzled as
+// the map says); completion is counted in bytes on `bar`.
+__device__ __forceinline__ void tma_gather4(uint32_t dst, const void *tmap, int x, int y0, int y1, int y2, int y3,
+                                            uint32_t bar)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes "
+        "[%0], [%1, {%2, %3, %4, %5, %6}], [%7];"
+        ::"r"(dst), "l"(reinterpret_cast<uint64_t>(tmap)), "r"(x), "r"(y0), "r"(y1), "r"(y2), "r"(y3), "r"(bar)
+        : "memory");
+}
+
+__device__ __forceinline__ void prefetch_tensormap(const void *tmap)
+{
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(tmap)) : "memory");
 }
 
 // ------------------------------------------------------------------ tcgen05: TMEM

@@ -39,7 +39,10 @@
 #include "va_internal.cuh"
 #include "tc_ptx.cuh"
 
+#include <cuda.h>
+#include <cudaTypedefs.h>
 #include <math.h>
+#include <mutex>
 
 namespace va {
 namespace {
@@ -49,10 +52,12 @@ using namespace ptx;
 constexpr int ROWS = 128;                  // rows per unit = M of every MMA
 constexpr int KEYS = 64;                   // keys per tile
 constexpr int STAGES = 3;                  // gathered tiles in flight per CTA
-constexpr int THREADS = 288;               // warps 0-3 rows, 4-7 gather, 8 MMA issue
-constexpr int PRODUCER_WARP0 = 4;
-constexpr int MMA_WARP = 8;
-constexpr int PRODUCERS = 128;
+constexpr int THREADS = 576;               // warps 0-7 rows, 8-15 gather (TMA), 16 MMA issue, 17 P sender
+constexpr int SOFTMAX_THREADS = 256;       // S role: two warp groups, each owns half the keys of a tile
+constexpr int PRODUCER_WARP0 = 8;          // TMA issue is serial within a warp, so 8 warps share it
+constexpr int PRODUCER_WARPS = 8;
+constexpr int MMA_WARP = 16;
+constexpr int SENDER_WARP = 17;
 constexpr uint32_t CHUNK_BYTES = KEYS * 128;          // one 64-dim column block of a tile
 constexpr uint32_t K_CHUNKS = D / 64;                 // 9
 constexpr uint32_t V_CHUNKS = DV / 64;                // 8
@@ -64,7 +69,8 @@ constexpr uint32_t STAGE0 = HEADER;                   // both roles: gathered ti
 constexpr uint32_t PBUF0 = HEADER + STAGES * V_STAGE; // O role: two P buffers
 constexpr uint32_t SMEM_USED = PBUF0 + 2 * P_BUF;
 constexpr uint32_t SMEM_ALLOC = SMEM_USED + 1024;     // room to align the base to 1 KB
-static_assert(STAGE0 + STAGES * K_STAGE <= SMEM_USED, "S role layout");
+constexpr uint32_t S_SCRATCH = STAGE0 + STAGES * K_STAGE; // S role: per-row partial sums of the 2nd group
+static_assert(S_SCRATCH + ROWS * 4 <= SMEM_USED, "S role layout");
 static_assert(SMEM_ALLOC <= 232448, "at most 227 KB of shared memory per CTA");
 
 constexpr uint32_t TMEM_COLS = 512;
@@ -80,14 +86,15 @@ constexpr uint64_t TIMEOUT_NS = 1000000000ull;
 // Shared-memory header at the (1 KB aligned) base; same offsets in both CTAs
 // so a barrier or field can be addressed in the partner with mapa.
 struct Header {
-    uint64_t k_full[STAGES];   // S: gathered K tile landed (128 cp.async arrivals + 4 warp leaders)
+    uint64_t k_full[STAGES];   // S: gathered K tile landed (8 producer-warp arrives + TMA bytes)
     uint64_t k_empty[STAGES];  // S: MMAs reading the stage completed (commit)
     uint64_t s_full[2];        // S: scores ready (commit) + valid-key bits published (MMA thread)
-    uint64_t s_free[2];        // S: 128 row threads have read the score buffer
+    uint64_t s_free[2];        // S: the 8 softmax warps have read the score buffer
+    uint64_t p_written[2];     // S: the 8 softmax warps stored a P tile into the partner
     uint64_t p_empty[2];       // S: partner done with a P buffer (its commit + its 4 row-warp leaders)
-    uint64_t v_full[STAGES];   // O: gathered V tile landed (128 cp.async arrivals)
+    uint64_t v_full[STAGES];   // O: gathered V tile landed (8 producer-warp arrives + TMA bytes)
     uint64_t v_empty[STAGES];  // O: MMAs reading the stage completed
-    uint64_t p_full[2];        // O: partner's 4 row warps wrote a P tile (one arrive per warp)
+    uint64_t p_full[2];        // O: partner's sender warp published a P tile
     uint64_t pv_sync;          // O: every MMA issued so far completed (before a rescale)
     uint64_t rs_req;           // O: MMA thread asks the row warps to rescale O
     uint64_t rs_done;          // O: 128 row threads rescaled their rows
@@ -157,59 +164,81 @@ __device__ __forceinline__ uint64_t load_bits(const uint8_t *mask, int64_t bit0,
     return w;
 }
 
-// ------------------------------------------------------------------ gather (warps 4-7, both roles)
+// ------------------------------------------------------------------ gather (warps 8-15, both roles)
 //
 // Tile layout in shared memory: NCH column blocks of 64 dims; block c holds
 // the 64 keys as 128-B rows (key n at n*128), 16-B pieces swizzled as
-// piece q -> q ^ (n & 7) inside each 1 KB group of 8 keys.  Read as B of
-// Q K^T it is K-major (rows = keys); read as B of P V it is MN-major (64
-// contiguous dims per key row, 8 keys per 1 KB group).
+// piece q -> q ^ (n & 7) inside each 1 KB group of 8 keys (the tensor map's
+// 128-byte swizzle).  Read as B of Q K^T it is K-major (rows = keys); read as
+// B of P V it is MN-major (64 contiguous dims per key row, 8 keys per 1 KB
+// group).  Producer warp w (0..7) owns keys 8w..8w+7: lanes 0 and 1 each
+// gather four keys with one TMA gather4 per column block (a warp issues its
+// TMA instructions one after another, so the tile is spread over 8 warps).
+// A key without a valid slot reads row pool_size, outside the map, which
+// TMA fills with zeros.  Slots are loaded two tiles ahead, without branches
+// on the loaded values, so the index loads overlap the stage waits.
 template <int NCH>
-__device__ void gather_tiles(const Params &p, Header *h, uint32_t stage_base, uint32_t stage_bytes,
-                             uint64_t *full, uint64_t *empty, uint64_t *valid, const Unit &u)
+__device__ void gather_tiles(const Params &p, Header *h, const CUtensorMap *tmap, uint32_t stage_base,
+                             uint32_t stage_bytes, uint64_t *full, uint64_t *empty, uint64_t *valid, const Unit &u)
 {
     const int pw = (int)(threadIdx.x >> 5) - PRODUCER_WARP0;
     const int lane = threadIdx.x & 31;
-    // Slot of key (pw*16 + lane) of tile t, or -1; resolved one tile ahead so
-    // the index load overlaps the wait for a free stage.
-    auto slot_of = [&](int t) -> int64_t {
-        const int64_t j = u.k0 + (int64_t)t * KEYS + pw * 16 + lane;
-        return (lane < 16 && t < u.ntiles && j < u.k1) ? key_slot(p, u.kv0, u.qo0, u.L, j) : -1;
+    const int64_t oob = p.pool_size;
+    struct Rows { int64_t s[4]; };
+    // Raw slots of this lane's 4 keys of tile t (-1 past the split or for idle lanes).
+    auto load_rows = [&](int t) -> Rows {
+        Rows r;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const int64_t j = u.k0 + (int64_t)t * KEYS + pw * 8 + lane * 4 + k;
+            const bool live = lane < 2 && t < u.ntiles && j < u.k1;
+            int64_t s = -1;
+            if (live) {
+                if (j < u.L) s = p.kv_indices ? (int64_t)__ldg(p.kv_indices + u.kv0 + j) : -2;
+                else s = p.out_cache_loc ? __ldg(p.out_cache_loc + u.qo0 + (j - u.L)) : -2;
+                if (s < 0 || s >= oob) s = -2;          // invalid slot: flagged, read as zeros
+            }
+            r.s[k] = s;
+        }
+        return r;
     };
-    int64_t next_slot = slot_of(0);
+    Rows ahead1 = load_rows(0), ahead2 = load_rows(1);
     for (int t = 0; t < u.ntiles; ++t) {
         const int stage = t % STAGES;
-        const int64_t slot = next_slot;
-        next_slot = slot_of(t + 1);
-        if (t >= STAGES && !wait_bar(h, smem_u32(&empty[stage]), (uint32_t)((t / STAGES) - 1) & 1u, p.status, false))
+        const Rows cur = ahead1;
+        ahead1 = ahead2;
+        ahead2 = load_rows(t + 2);
+        if (t >= STAGES &&
+            !__all_sync(0xffffffffu, wait_bar(h, smem_u32(&empty[stage]), (uint32_t)((t / STAGES) - 1) & 1u, p.status, false)))
             break;
-        const uint32_t ok = __ballot_sync(0xffffffffu, lane < 16 && slot >= 0) & 0xFFFFu;
-        const uint32_t sb = stage_base + (uint32_t)stage * stage_bytes;
-#pragma unroll 1
-        for (int kk = 0; kk < 16; ++kk) {
-            const int64_t s = __shfl_sync(0xffffffffu, slot, kk);
-            const int n = pw * 16 + kk;
-            const __nv_bfloat16 *src = p.kv_pool + (s >= 0 ? s : 0) * D;
-            const uint32_t bytes = s >= 0 ? 16u : 0u;
-            const uint32_t row = sb + (uint32_t)n * 128u;
+        uint32_t nib = 0, bad = 0;
+        int y[4];
 #pragma unroll
-            for (int piece = lane; piece < NCH * 8; piece += 32) {
-                const uint32_t c = (uint32_t)piece >> 3, q = (uint32_t)piece & 7u;
-                cp_async16(row + c * CHUNK_BYTES + ((q ^ ((uint32_t)n & 7u)) << 4), src + piece * 8, bytes);
-            }
+        for (int k = 0; k < 4; ++k) {
+            nib |= (cur.s[k] >= 0 ? 1u : 0u) << k;
+            bad |= cur.s[k] == -2 ? 1u : 0u;
+            y[k] = cur.s[k] >= 0 ? (int)cur.s[k] : (int)oob;
         }
-        cp_async_arrive_noinc(smem_u32(&full[stage]));
-        if (valid != nullptr && lane == 0) {
-            reinterpret_cast<volatile uint16_t *>(&valid[stage])[pw] = (uint16_t)ok;
-            mbar_arrive(smem_u32(&full[stage]));
+        if (bad) atomicOr(p.status, STATUS_BAD_SLOT);
+        const uint32_t nib1 = __shfl_sync(0xffffffffu, nib, 1);
+        const uint32_t bar = smem_u32(&full[stage]);
+        if (lane == 0) {
+            if (valid != nullptr)
+                reinterpret_cast<volatile uint8_t *>(&valid[stage])[pw] = (uint8_t)(nib | (nib1 << 4));
+            if (pw == 0) mbar_arrive_expect_tx(bar, NCH * CHUNK_BYTES);
+            else mbar_arrive(bar);
+        }
+        if (lane < 2) {
+            const uint32_t dst = stage_base + (uint32_t)stage * stage_bytes + (uint32_t)(pw * 2 + lane) * 512u;
+#pragma unroll
+            for (int c = 0; c < NCH; ++c) tma_gather4(dst + c * CHUNK_BYTES, tmap, c * 64, y[0], y[1], y[2], y[3], bar);
         }
     }
-    cp_async_wait_all();
 }
 
 // ------------------------------------------------------------------ S role
 
-// MMA issue (warp 8, lane 0): S[buf] = Q K^T for every tile.
+// MMA issue (warp 16, lane 0): S[buf] = Q K^T for every tile.
 __device__ void s_role_mma(const Params &p, Header *h, uint32_t smem, uint32_t tmem, const Unit &u)
 {
     for (int t = 0; t < u.ntiles; ++t) {
@@ -217,8 +246,7 @@ __device__ void s_role_mma(const Params &p, Header *h, uint32_t smem, uint32_t t
         if (!wait_bar(h, smem_u32(&h->k_full[stage]), (uint32_t)(t / STAGES) & 1u, p.status, false)) break;
         if (t >= 2 && !wait_bar(h, smem_u32(&h->s_free[buf]), (uint32_t)((t >> 1) - 1) & 1u, p.status, false))
             break;
-        tc_fence_after_sync();
-        fence_proxy_async_smem();
+        tc_fence_after_sync();   // K arrives by TMA (async proxy): no proxy fence needed before the MMAs
         *reinterpret_cast<volatile uint64_t *>(&h->s_valid[buf]) =
             *reinterpret_cast<volatile uint64_t *>(&h->k_valid[stage]);
         const uint32_t kb = smem + STAGE0 + (uint32_t)stage * K_STAGE;
@@ -236,12 +264,18 @@ __device__ void s_role_mma(const Params &p, Header *h, uint32_t smem, uint32_t t
     wait_bar(h, smem_u32(&h->drain), 0u, p.status, false, false);
 }
 
-// Row warps (thread = row): Q into TMEM, then per tile mask + online softmax
-// + P to the partner; finally lse to the workspace and 1/l to the partner.
+// Softmax warps 0-7 (thread = row; warp group g = warp / 4 owns keys
+// [32g, 32g + 32) of every tile).  Both groups read the full score row and
+// compute the same running maximum, so they agree on every rescale without
+// exchanging data; each exponentiates and ships only its own 32 keys.  Q goes
+// into TMEM first; after the last tile the groups add their partial sums,
+// group 0 writes the lse to the workspace and 1/l to the partner.
 __device__ void s_role_rows(const Params &p, Header *h, uint32_t smem, uint32_t tmem, const Unit &u)
 {
-    const int r = threadIdx.x, warp = r >> 5, lane = r & 31;
-    const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int quad = warp & 3, grp = warp >> 2;
+    const int r = quad * 32 + lane;
+    const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
     const int H = p.num_heads;
     const int64_t lr = u.r0 + r;
     const bool row_ok = lr < u.rows_b;
@@ -249,9 +283,10 @@ __device__ void s_role_rows(const Params &p, Header *h, uint32_t smem, uint32_t 
     const int64_t hh = row_ok ? lr % H : 0;
 
     // Q row -> TMEM columns [0, 288): 32-bit column k/2 holds elements k, k+1.
+    // Group 0 writes dims 0..319, group 1 dims 320..575.
     const __nv_bfloat16 *qrow = p.q + (u.qo0 + i) * p.q_stride_tok + hh * p.q_stride_head;
 #pragma unroll 1
-    for (int c = 0; c < D / 64; ++c) {
+    for (int c = grp * 5; c < (grp ? D / 64 : 5); ++c) {
         uint32_t w[32];
 #pragma unroll
         for (int v = 0; v < 8; ++v) {
@@ -263,7 +298,7 @@ __device__ void s_role_rows(const Params &p, Header *h, uint32_t smem, uint32_t 
     }
     tmem_st_wait();
     tc_fence_before_sync();
-    named_barrier_sync(1, 160);
+    named_barrier_sync(1, SOFTMAX_THREADS + 32);
 
     const int64_t mrow = p.mask_indptr[u.b] + i * u.N;
     const float sl2 = p.sm_scale * LOG2E;
@@ -286,24 +321,40 @@ __device__ void s_role_rows(const Params &p, Header *h, uint32_t smem, uint32_t 
         next_bits = mask_of(t + 1);
         if (!warp_wait(h, smem_u32(&h->s_full[buf]), (uint32_t)(t >> 1) & 1u, p.status, false)) { ok = false; break; }
         tc_fence_after_sync();
-        uint32_t sa[32], sb[32];
-        tmem_ld32(tmem + lane_base + TM_S0 + 64u * (uint32_t)buf, sa);
-        tmem_ld32(tmem + lane_base + TM_S0 + 64u * (uint32_t)buf + 32u, sb);
+        // The other group's 32 scores first (only their maximum is kept), then
+        // this group's own 32; raw scores, the scale is folded into the exponent.
+        const uint64_t vis = *reinterpret_cast<volatile uint64_t *>(&h->s_valid[buf]) & bits;
+        const uint32_t s_col = tmem + lane_base + TM_S0 + 64u * (uint32_t)buf;
+        const uint32_t v_own = (uint32_t)(vis >> (32 * grp)), v_oth = (uint32_t)(vis >> (32 * (1 - grp)));
+        const bool all_vis = __all_sync(0xffffffffu, vis == ~0ull);
+        uint32_t sv[32];
+        float mx = -INFINITY;
+        tmem_ld32(s_col + 32u * (uint32_t)(1 - grp), sv);
+        tmem_ld_wait();
+        if (all_vis) {
+#pragma unroll
+            for (int n = 0; n < 32; ++n) mx = fmaxf(mx, __uint_as_float(sv[n]));
+        } else {
+#pragma unroll
+            for (int n = 0; n < 32; ++n) mx = fmaxf(mx, ((v_oth >> n) & 1u) ? __uint_as_float(sv[n]) : -INFINITY);
+        }
+        tmem_ld32(s_col + 32u * (uint32_t)grp, sv);
         tmem_ld_wait();
         tc_fence_before_sync();
-        mbar_arrive(smem_u32(&h->s_free[buf]));
-
-        const uint64_t vis = *reinterpret_cast<volatile uint64_t *>(&h->s_valid[buf]) & bits;
-
-        float mx = -INFINITY;
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&h->s_free[buf]));
+        if (all_vis) {
 #pragma unroll
-        for (int n = 0; n < 32; ++n) {
-            const float s0 = ((vis >> n) & 1ull) ? __uint_as_float(sa[n]) * sl2 : -INFINITY;
-            const float s1 = ((vis >> (n + 32)) & 1ull) ? __uint_as_float(sb[n]) * sl2 : -INFINITY;
-            sa[n] = __float_as_uint(s0);
-            sb[n] = __float_as_uint(s1);
-            mx = fmaxf(mx, fmaxf(s0, s1));
+            for (int n = 0; n < 32; ++n) mx = fmaxf(mx, __uint_as_float(sv[n]));
+        } else {
+#pragma unroll
+            for (int n = 0; n < 32; ++n) {
+                const float x = ((v_own >> n) & 1u) ? __uint_as_float(sv[n]) : -INFINITY;
+                sv[n] = __float_as_uint(x);
+                mx = fmaxf(mx, x);
+            }
         }
+        mx *= sl2;                                 // maximum in log2 units (sl2 > 0 keeps the order)
         float alpha = 1.f;
         bool rescale = false;
         if (mx > m_used + RESCALE_LOG2) {        // also the first tile where the row sees a key
@@ -316,35 +367,40 @@ __device__ void s_role_rows(const Params &p, Header *h, uint32_t smem, uint32_t 
             ok = false;
             break;
         }
-        uint32_t pk[32];
+        // p = 2^(s * sl2 - m_used); masked scores are -inf and give exactly 0.
+        const float neg_m = m_used == -INFINITY ? 0.f : -m_used;
+        uint32_t pk[16];
         float psum = 0.f;
 #pragma unroll
         for (int n = 0; n < 16; ++n) {
-            const float a0 = __uint_as_float(sa[2 * n]), a1 = __uint_as_float(sa[2 * n + 1]);
-            const float b0 = __uint_as_float(sb[2 * n]), b1 = __uint_as_float(sb[2 * n + 1]);
-            const float pa0 = a0 == -INFINITY ? 0.f : ex2_approx(a0 - m_used);
-            const float pa1 = a1 == -INFINITY ? 0.f : ex2_approx(a1 - m_used);
-            const float pb0 = b0 == -INFINITY ? 0.f : ex2_approx(b0 - m_used);
-            const float pb1 = b1 == -INFINITY ? 0.f : ex2_approx(b1 - m_used);
-            psum += (pa0 + pa1) + (pb0 + pb1);
-            pk[n] = pack_bf16x2(pa0, pa1);
-            pk[16 + n] = pack_bf16x2(pb0, pb1);
+            const float p0 = ex2_approx(fmaf(__uint_as_float(sv[2 * n]), sl2, neg_m));
+            const float p1 = ex2_approx(fmaf(__uint_as_float(sv[2 * n + 1]), sl2, neg_m));
+            psum += p0 + p1;
+            pk[n] = pack_bf16x2(p0, p1);
         }
         l += psum;
-        // Row r of the partner's P buffer: K-major, 128-B swizzle (A of P V).
+        // Row r of the partner's P buffer: K-major, 128-B swizzle (A of P V);
+        // this group's 32 keys are 16-B pieces 4g .. 4g+3 of the row.
         const uint32_t prow = peer_pbuf + (uint32_t)buf * P_BUF + (uint32_t)(r >> 3) * 1024u + (uint32_t)(r & 7) * 128u;
 #pragma unroll
-        for (int q = 0; q < 8; ++q)
-            st_cluster_v4(prow + (((uint32_t)q ^ (uint32_t)(r & 7)) << 4), pk[4 * q], pk[4 * q + 1], pk[4 * q + 2],
-                          pk[4 * q + 3]);
-        st_cluster_f32(peer_alpha + (uint32_t)(buf * ROWS + r) * 4u, rescale ? alpha : 1.f);
-        const uint32_t any = __any_sync(0xffffffffu, rescale) ? 1u : 0u;
-        if (lane == 0) st_cluster_u8(peer_flags + (uint32_t)buf * 4u + (uint32_t)warp, any);
-        fence_proxy_async_cluster();
+        for (int q = 0; q < 4; ++q)
+            st_cluster_v4(prow + ((((uint32_t)(4 * grp + q)) ^ (uint32_t)(r & 7)) << 4), pk[4 * q], pk[4 * q + 1],
+                          pk[4 * q + 2], pk[4 * q + 3]);
+        if (grp == 0) {
+            st_cluster_f32(peer_alpha + (uint32_t)(buf * ROWS + r) * 4u, rescale ? alpha : 1.f);
+            const uint32_t any = __any_sync(0xffffffffu, rescale) ? 1u : 0u;
+            if (lane == 0) st_cluster_u8(peer_flags + (uint32_t)buf * 4u + (uint32_t)quad, any);
+        }
         __syncwarp();
-        if (lane == 0) mbar_arrive_cluster(smem_u32(&h->p_full[buf]), 1);
+        if (lane == 0) mbar_arrive(smem_u32(&h->p_written[buf]));
     }
 
+    // Partial sums of group 1 -> group 0 (both groups always reach this barrier).
+    float *lpart = reinterpret_cast<float *>(reinterpret_cast<uint8_t *>(h) + S_SCRATCH);
+    if (grp == 1) lpart[r] = l;
+    named_barrier_sync(2, SOFTMAX_THREADS);
+    if (grp == 1) return;
+    l += lpart[r];
     if (ok && row_ok) {
         const int64_t row = u.qo0 * H + lr;
         if (row < p.rows_cap)
@@ -355,9 +411,23 @@ __device__ void s_role_rows(const Params &p, Header *h, uint32_t smem, uint32_t 
     if (lane == 0) mbar_arrive_cluster(smem_u32(&h->l_ready), 1);
 }
 
+// Sender (warp 17, lane 0): once all 8 softmax warps stored a P tile into the
+// partner, order those writes for the partner's tensor-core reads and
+// publish the tile.  Keeps the proxy fence and the cluster-scope release off
+// the softmax warps.
+__device__ void s_role_sender(const Params &p, Header *h, const Unit &u)
+{
+    for (int t = 0; t < u.ntiles; ++t) {
+        const int buf = t & 1;
+        if (!wait_bar(h, smem_u32(&h->p_written[buf]), (uint32_t)(t >> 1) & 1u, p.status, false)) break;
+        fence_proxy_async_cluster();
+        mbar_arrive_cluster(smem_u32(&h->p_full[buf]), 1);
+    }
+}
+
 // ------------------------------------------------------------------ O role
 
-// MMA issue (warp 8, lane 0): O += P V for every tile, both 256-column halves.
+// MMA issue (warp 16, lane 0): O += P V for every tile, both 256-column halves.
 __device__ void o_role_mma(const Params &p, Header *h, uint32_t smem, uint32_t tmem, const Unit &u)
 {
     uint32_t nrs = 0;
@@ -453,7 +523,8 @@ __device__ void o_role_rows(const Params &p, Header *h, uint32_t smem, uint32_t 
     }
 }
 
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1) tc_split_kernel(Params p)
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
+    tc_split_kernel(Params p, const __grid_constant__ CUtensorMap pool_map)
 {
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
@@ -490,16 +561,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1) tc_split
 
     if (tid == 0) {
         for (int s = 0; s < STAGES; ++s) {
-            mbar_init(smem_u32(&h->k_full[s]), PRODUCERS + 4);
+            mbar_init(smem_u32(&h->k_full[s]), PRODUCER_WARPS);
             mbar_init(smem_u32(&h->k_empty[s]), 1);
-            mbar_init(smem_u32(&h->v_full[s]), PRODUCERS);
+            mbar_init(smem_u32(&h->v_full[s]), PRODUCER_WARPS);
             mbar_init(smem_u32(&h->v_empty[s]), 1);
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(smem_u32(&h->s_full[i]), 2);
-            mbar_init(smem_u32(&h->s_free[i]), ROWS);
+            mbar_init(smem_u32(&h->s_free[i]), SOFTMAX_THREADS / 32);
+            mbar_init(smem_u32(&h->p_written[i]), SOFTMAX_THREADS / 32);
             mbar_init(smem_u32(&h->p_empty[i]), 1 + 4);
-            mbar_init(smem_u32(&h->p_full[i]), 4);
+            mbar_init(smem_u32(&h->p_full[i]), 1);
             h->flags[i] = 0u;
         }
         mbar_init(smem_u32(&h->pv_sync), 1);
@@ -510,6 +582,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1) tc_split
         h->abort = 0u;
         fence_mbar_init_cluster();
     }
+    if (warp == PRODUCER_WARP0 && lane == 0) prefetch_tensormap(&pool_map);
     if (warp == MMA_WARP) {
         tmem_alloc(smem_u32(&h->tmem_base), TMEM_COLS);
         tmem_relinquish();
@@ -521,21 +594,23 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1) tc_split
     const uint32_t tmem = *reinterpret_cast<volatile uint32_t *>(&h->tmem_base);
 
     if (role == 0) {
-        if (warp < 4) {
+        if (warp < PRODUCER_WARP0) {
             s_role_rows(p, h, smem, tmem, u);
         } else if (warp < MMA_WARP) {
-            gather_tiles<K_CHUNKS>(p, h, smem + STAGE0, K_STAGE, h->k_full, h->k_empty, h->k_valid, u);
-        } else {
-            named_barrier_sync(1, 160);
+            gather_tiles<K_CHUNKS>(p, h, &pool_map, smem + STAGE0, K_STAGE, h->k_full, h->k_empty, h->k_valid, u);
+        } else if (warp == MMA_WARP) {
+            named_barrier_sync(1, SOFTMAX_THREADS + 32);
             tc_fence_after_sync();
             if (lane == 0) s_role_mma(p, h, smem, tmem, u);
+        } else if (lane == 0) {
+            s_role_sender(p, h, u);
         }
     } else {
         if (warp < 4) {
             o_role_rows(p, h, smem, tmem, u);
-        } else if (warp < MMA_WARP) {
-            gather_tiles<V_CHUNKS>(p, h, smem + STAGE0, V_STAGE, h->v_full, h->v_empty, nullptr, u);
-        } else if (lane == 0) {
+        } else if (warp >= PRODUCER_WARP0 && warp < MMA_WARP) {
+            gather_tiles<V_CHUNKS>(p, h, &pool_map, smem + STAGE0, V_STAGE, h->v_full, h->v_empty, nullptr, u);
+        } else if (warp == MMA_WARP && lane == 0) {
             o_role_mma(p, h, smem, tmem, u);
         }
     }
@@ -550,20 +625,49 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1) tc_split
     }
 }
 
+
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::once_flag g_encode_once;
+
+// 2-D tensor map over the pool [pool_size rows, 576 bf16]: box of 64
+// columns x 1 row (the gather4 form), 128-byte swizzle, zero fill outside.
+bool encode_pool_map(const Params &p, CUtensorMap *map)
+{
+    if (g_encode == nullptr || p.pool_size >= ((int64_t)1 << 31)) return false;
+    const cuuint64_t dims[2] = {(cuuint64_t)D, (cuuint64_t)p.pool_size};
+    const cuuint64_t strides[1] = {(cuuint64_t)D * sizeof(__nv_bfloat16)};
+    const cuuint32_t box[2] = {64, 1};
+    const cuuint32_t estr[2] = {1, 1};
+    return g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<__nv_bfloat16 *>(p.kv_pool), dims, strides,
+                    box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 }  // namespace
 
 cudaError_t tc_init()
 {
+    std::call_once(g_encode_once, [] {
+        void *fn = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    });
+    if (g_encode == nullptr) return cudaErrorNotSupported;
     return cudaFuncSetAttribute(tc_split_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_ALLOC);
 }
 
-bool tc_supported(const Params &) { return true; }
+bool tc_supported(const Params &p) { return p.pool_size < ((int64_t)1 << 31); }
 
 cudaError_t launch_tc_split(const Params &p, cudaStream_t stream)
 {
+    CUtensorMap map;
+    if (!encode_pool_map(p, &map)) return cudaErrorInvalidValue;
     const int row_tiles = (int)((p.max_q_per_req * (int64_t)p.num_heads + ROWS - 1) / ROWS);
     dim3 grid(2u * (unsigned)row_tiles, (unsigned)p.num_splits, (unsigned)p.batch);
-    tc_split_kernel<<<grid, THREADS, SMEM_ALLOC, stream>>>(p);
+    tc_split_kernel<<<grid, THREADS, SMEM_ALLOC, stream>>>(p, map);
     return cudaGetLastError();
 }
 
