@@ -133,7 +133,7 @@ VERIFY_ATTN_API int verify_attn_init(void);
  *                the launch grid (so one captured graph serves every batch
  *                with these bounds).  Request b's keys are cut into chunks of
  *                c_b = max(ceil(N_b/num_splits), 256) rounded up to a multiple
- *                of 64; splits past the end exit at once (Decision 3).
+ *                of 128; splits past the end exit at once (Decision 3).
  *   workspace    device scratch of workspace_bytes (see above), 256-B aligned.
  *
  * The index buffers and the mask are read in place, inside the kernels; the

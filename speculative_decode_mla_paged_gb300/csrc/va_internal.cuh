@@ -10,7 +10,7 @@ namespace va {
 
 constexpr int D = 576;            // latent row: 512 no-PE + 64 RoPE dims
 constexpr int DV = 512;           // V = first 512 dims of the row
-constexpr int KEY_ALIGN = 64;     // split chunks are multiples of this many keys
+constexpr int KEY_ALIGN = 128;    // split chunks are multiples of this many keys
 constexpr int MIN_CHUNK = 256;    // and at least this long (a split reloads its query tile)
 constexpr size_t WS_HEADER = 256; // status word + padding at the workspace start
 

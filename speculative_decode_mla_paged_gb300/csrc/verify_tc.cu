@@ -50,8 +50,11 @@ namespace {
 using namespace ptx;
 
 constexpr int ROWS = 128;                  // rows per unit = M of every MMA
-constexpr int KEYS = 64;                   // keys per tile
-constexpr int STAGES = 3;                  // gathered tiles in flight per CTA
+constexpr int KEYS = 64;                   // keys per O-role tile (one P half)
+constexpr int KEYS_S = 128;                // keys per S-role tile (N of the score MMAs)
+constexpr int STAGES = 3;                  // O role: gathered V tiles in flight
+constexpr int NSLOT = 4;                   // S role: ring of 48 KB slots, 3 K chunks (128 keys x 64 dims) each
+constexpr int SLOT_CHUNKS = 3;
 constexpr int THREADS = 576;               // warps 0-7 rows, 8-15 gather (TMA), 16 MMA issue, 17 P sender
 constexpr int SOFTMAX_THREADS = 256;       // S role: two warp groups, each owns half the keys of a tile
 constexpr int PRODUCER_WARP0 = 8;          // TMA issue is serial within a warp, so 8 warps share it
@@ -61,7 +64,8 @@ constexpr int SENDER_WARP = 17;
 constexpr uint32_t CHUNK_BYTES = KEYS * 128;          // one 64-dim column block of a tile
 constexpr uint32_t K_CHUNKS = D / 64;                 // 9
 constexpr uint32_t V_CHUNKS = DV / 64;                // 8
-constexpr uint32_t K_STAGE = K_CHUNKS * CHUNK_BYTES;  // 73728
+constexpr uint32_t KCHUNK_BYTES = KEYS_S * 128;       // 16384: one K chunk of an S tile
+constexpr uint32_t SLOT_BYTES = SLOT_CHUNKS * KCHUNK_BYTES;
 constexpr uint32_t V_STAGE = V_CHUNKS * CHUNK_BYTES;  // 65536
 constexpr uint32_t P_BUF = ROWS * KEYS * 2;           // 16384
 constexpr uint32_t HEADER = 2048;
@@ -69,14 +73,16 @@ constexpr uint32_t STAGE0 = HEADER;                   // both roles: gathered ti
 constexpr uint32_t PBUF0 = HEADER + STAGES * V_STAGE; // O role: two P buffers
 constexpr uint32_t SMEM_USED = PBUF0 + 2 * P_BUF;
 constexpr uint32_t SMEM_ALLOC = SMEM_USED + 1024;     // room to align the base to 1 KB
-constexpr uint32_t S_SCRATCH = STAGE0 + STAGES * K_STAGE; // S role: per-row partial sums of the 2nd group
+constexpr uint32_t QPE0 = HEADER;                     // S role: Q's 64 RoPE dims, 128 x 128 B (A of 4 MMAs)
+constexpr uint32_t RING0 = QPE0 + ROWS * 128;         // S role: K chunk ring
+constexpr uint32_t S_SCRATCH = RING0 + NSLOT * SLOT_BYTES; // S role: per-row partial sums of the 2nd group
 static_assert(S_SCRATCH + ROWS * 4 <= SMEM_USED, "S role layout");
 static_assert(SMEM_ALLOC <= 232448, "at most 227 KB of shared memory per CTA");
 
 constexpr uint32_t TMEM_COLS = 512;
-constexpr uint32_t TM_Q = 0;                          // S role: 288 columns
-constexpr uint32_t TM_S0 = 320;                       // S role: S buffers at 320 and 384
-constexpr uint32_t IDESC_S = idesc_bf16(128, 64, false);
+constexpr uint32_t TM_Q = 0;                          // S role: Q's 512 no-PE dims, 256 columns
+constexpr uint32_t TM_S0 = 256;                       // S role: S buffers at 256 and 384 (128 columns each)
+constexpr uint32_t IDESC_S = idesc_bf16(128, 128, false);
 constexpr uint32_t IDESC_PV = idesc_bf16(128, 256, true);
 constexpr float LOG2E = 1.4426950408889634f;
 constexpr float LN2 = 0.69314718055994531f;
@@ -86,11 +92,11 @@ constexpr uint64_t TIMEOUT_NS = 1000000000ull;
 // Shared-memory header at the (1 KB aligned) base; same offsets in both CTAs
 // so a barrier or field can be addressed in the partner with mapa.
 struct Header {
-    uint64_t k_full[STAGES];   // S: gathered K tile landed (8 producer-warp arrives + TMA bytes)
-    uint64_t k_empty[STAGES];  // S: MMAs reading the stage completed (commit)
+    uint64_t c_full[NSLOT];    // S: 3 K chunks landed in a ring slot (8 producer-warp arrives + TMA bytes)
+    uint64_t c_empty[NSLOT];   // S: MMAs reading the slot completed (commit)
     uint64_t s_full[2];        // S: scores ready (commit) + valid-key bits published (MMA thread)
     uint64_t s_free[2];        // S: the 8 softmax warps have read the score buffer
-    uint64_t p_written[2];     // S: the 8 softmax warps stored a P tile into the partner
+    uint64_t p_written[2];     // S: softmax group g (4 warps) stored its P half into the partner's buffer g
     uint64_t p_empty[2];       // S: partner done with a P buffer (its commit + its 4 row-warp leaders)
     uint64_t v_full[STAGES];   // O: gathered V tile landed (8 producer-warp arrives + TMA bytes)
     uint64_t v_empty[STAGES];  // O: MMAs reading the stage completed
@@ -100,8 +106,8 @@ struct Header {
     uint64_t rs_done;          // O: 128 row threads rescaled their rows
     uint64_t l_ready;          // O: partner's 4 row warps wrote 1/l
     uint64_t drain;            // both: all MMAs of the CTA completed
-    uint64_t k_valid[STAGES];  // S: bit n = key n of the stage has a valid slot
-    uint64_t s_valid[2];       // S: the same bits, per score buffer
+    uint64_t t_valid[2][2];    // S: bit n of an S tile's 128 keys = key n has a valid slot (tile ring of 2)
+    uint64_t s_valid[2][2];    // S: the same bits, per score buffer
     uint32_t tmem_base;
     uint32_t abort;
     uint32_t flags[2];         // O: byte w != 0 if a row of warp w rescales on this P buffer
@@ -113,8 +119,27 @@ static_assert(sizeof(Header) <= HEADER, "header fits");
 struct Unit {
     int split, b;
     int64_t qo0, kv0, L, N, k0, k1, r0, rows_b;
-    int ntiles;
+    int ntiles_s;              // S tiles of 128 keys
+    int ntiles;                // O tiles of 64 keys = 2 * ntiles_s (the last may be empty)
+    int rot;                   // this pair starts at S tile `rot` of its split (see tile_key0)
 };
+
+// First key of the t-th S tile this pair processes.  The row tiles of one
+// request read the same keys; each starts at a different tile of the split
+// (rot = row tile * ntiles_s / row tiles) so they do not request the same
+// rows from L2 at the same moment.  Softmax order does not change the result.
+__device__ __forceinline__ int64_t tile_key0(const Unit &u, int t)
+{
+    int s = t + u.rot;
+    if (s >= u.ntiles_s) s -= u.ntiles_s;
+    return u.k0 + (int64_t)s * KEYS_S;
+}
+
+// First key of the u-th O tile (64 keys: the two halves of each S tile).
+__device__ __forceinline__ int64_t otile_key0(const Unit &u, int t)
+{
+    return tile_key0(u, t >> 1) + (int64_t)(t & 1) * KEYS;
+}
 
 // Bounded wait on phase `parity` of a barrier.  False after a timeout (status
 // bit set, abort flag raised) or when another thread of the CTA aborted.
@@ -190,7 +215,7 @@ __device__ void gather_tiles(const Params &p, Header *h, const CUtensorMap *tmap
         Rows r;
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
-            const int64_t j = u.k0 + (int64_t)t * KEYS + pw * 8 + lane * 4 + k;
+            const int64_t j = (t < u.ntiles ? otile_key0(u, t) : 0) + pw * 8 + lane * 4 + k;
             const bool live = lane < 2 && t < u.ntiles && j < u.k1;
             int64_t s = -1;
             if (live) {
@@ -237,26 +262,117 @@ __device__ void gather_tiles(const Params &p, Header *h, const CUtensorMap *tmap
 }
 
 // ------------------------------------------------------------------ S role
+//
+// An S tile is 128 keys.  Its K rows reach shared memory as nine 16 KB
+// chunks (128 keys x 64 dims, same 128-byte swizzled key-row layout as the
+// V tiles), three chunks per slot of a 4-slot ring with one barrier pair per
+// slot, so the score MMAs (N = 128, the shape that runs at full tensor rate)
+// can start on a tile's first chunks while its later chunks are in flight.
 
-// MMA issue (warp 16, lane 0): S[buf] = Q K^T for every tile.
+// Gather (warps 8-15): producer warp w owns keys 16w..16w+15 of each S tile;
+// lanes 0-3 each gather four keys, one TMA gather4 per chunk.
+__device__ void s_role_gather(const Params &p, Header *h, const CUtensorMap *tmap, uint32_t smem, const Unit &u)
+{
+    const int pw = (int)(threadIdx.x >> 5) - PRODUCER_WARP0;
+    const int lane = threadIdx.x & 31;
+    const int64_t oob = p.pool_size;
+    struct Rows { int64_t s[4]; };
+    auto load_rows = [&](int t) -> Rows {
+        Rows r;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const int64_t j = (t < u.ntiles_s ? tile_key0(u, t) : 0) + pw * 16 + lane * 4 + k;
+            const bool live = lane < 4 && t < u.ntiles_s && j < u.k1;
+            int64_t s = -1;
+            if (live) {
+                if (j < u.L) s = p.kv_indices ? (int64_t)__ldg(p.kv_indices + u.kv0 + j) : -2;
+                else s = p.out_cache_loc ? __ldg(p.out_cache_loc + u.qo0 + (j - u.L)) : -2;
+                if (s < 0 || s >= oob) s = -2;          // invalid slot: flagged, read as zeros
+            }
+            r.s[k] = s;
+        }
+        return r;
+    };
+    Rows ahead1 = load_rows(0), ahead2 = load_rows(1);
+    for (int t = 0; t < u.ntiles_s; ++t) {
+        const Rows cur = ahead1;
+        ahead1 = ahead2;
+        ahead2 = load_rows(t + 2);
+        uint32_t nib = 0, bad = 0;
+        int y[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            nib |= (cur.s[k] >= 0 ? 1u : 0u) << k;
+            bad |= cur.s[k] == -2 ? 1u : 0u;
+            y[k] = cur.s[k] >= 0 ? (int)cur.s[k] : (int)oob;
+        }
+        if (bad) atomicOr(p.status, STATUS_BAD_SLOT);
+        uint32_t bits16 = 0;
+#pragma unroll
+        for (int l = 0; l < 4; ++l) bits16 |= __shfl_sync(0xffffffffu, nib, l) << (4 * l);
+        bool ok = true;
+        for (int gi = 0; gi < (int)K_CHUNKS / SLOT_CHUNKS; ++gi) {
+            const int q = t * ((int)K_CHUNKS / SLOT_CHUNKS) + gi, slot = q % NSLOT, use = q / NSLOT;
+            if (use > 0 &&
+                !__all_sync(0xffffffffu, wait_bar(h, smem_u32(&h->c_empty[slot]), (uint32_t)(use - 1) & 1u, p.status, false))) {
+                ok = false;
+                break;
+            }
+            const uint32_t bar = smem_u32(&h->c_full[slot]);
+            if (lane == 0) {
+                if (gi == 0) reinterpret_cast<volatile uint16_t *>(&h->t_valid[t & 1][0])[pw] = (uint16_t)bits16;
+                if (pw == 0) mbar_arrive_expect_tx(bar, SLOT_BYTES);
+                else mbar_arrive(bar);
+            }
+            if (lane < 4) {
+                const uint32_t dst = smem + RING0 + (uint32_t)slot * SLOT_BYTES + (uint32_t)(pw * 4 + lane) * 512u;
+#pragma unroll
+                for (int cc = 0; cc < SLOT_CHUNKS; ++cc)
+                    tma_gather4(dst + (uint32_t)cc * KCHUNK_BYTES, tmap, (gi * SLOT_CHUNKS + cc) * 64, y[0], y[1], y[2],
+                                y[3], bar);
+            }
+        }
+        if (!ok) break;
+    }
+}
+
+// MMA issue (warp 16, lane 0): S[buf] = Q K^T per S tile, chunk by chunk:
+// 32 MMAs with Q's no-PE dims from TMEM, then 4 with Q's RoPE dims from
+// shared memory; each chunk's slot is released by a commit.
 __device__ void s_role_mma(const Params &p, Header *h, uint32_t smem, uint32_t tmem, const Unit &u)
 {
-    for (int t = 0; t < u.ntiles; ++t) {
-        const int stage = t % STAGES, buf = t & 1;
-        if (!wait_bar(h, smem_u32(&h->k_full[stage]), (uint32_t)(t / STAGES) & 1u, p.status, false)) break;
-        if (t >= 2 && !wait_bar(h, smem_u32(&h->s_free[buf]), (uint32_t)((t >> 1) - 1) & 1u, p.status, false))
-            break;
-        tc_fence_after_sync();   // K arrives by TMA (async proxy): no proxy fence needed before the MMAs
-        *reinterpret_cast<volatile uint64_t *>(&h->s_valid[buf]) =
-            *reinterpret_cast<volatile uint64_t *>(&h->k_valid[stage]);
-        const uint32_t kb = smem + STAGE0 + (uint32_t)stage * K_STAGE;
-        const uint32_t d = tmem + TM_S0 + 64u * (uint32_t)buf;
-#pragma unroll 4
-        for (int k = 0; k < D / 16; ++k) {
-            const uint64_t bdesc = sdesc_sw128(kb + (uint32_t)(k >> 2) * CHUNK_BYTES + (uint32_t)(k & 3) * 32u, 16u, 1024u);
-            mma_ts(d, tmem + TM_Q + 8u * (uint32_t)k, bdesc, IDESC_S, k > 0 ? 1u : 0u);
+    for (int t = 0; t < u.ntiles_s; ++t) {
+        const int buf = t & 1;
+        if (t >= 2 && !wait_bar(h, smem_u32(&h->s_free[buf]), (uint32_t)((t >> 1) - 1) & 1u, p.status, false)) break;
+        const uint32_t d = tmem + TM_S0 + 128u * (uint32_t)buf;
+        bool ok = true;
+        for (int c = 0; c < (int)K_CHUNKS; ++c) {
+            const int q = t * ((int)K_CHUNKS / SLOT_CHUNKS) + c / SLOT_CHUNKS, slot = q % NSLOT, use = q / NSLOT;
+            if (c % SLOT_CHUNKS == 0) {
+                if (!wait_bar(h, smem_u32(&h->c_full[slot]), (uint32_t)use & 1u, p.status, false)) { ok = false; break; }
+                tc_fence_after_sync();   // K arrives by TMA (async proxy): no proxy fence needed before the MMAs
+            }
+            if (c == 0) {
+                volatile uint64_t *src = &h->t_valid[t & 1][0];
+                volatile uint64_t *dst = &h->s_valid[buf][0];
+                dst[0] = src[0];
+                dst[1] = src[1];
+            }
+            const uint32_t sb = smem + RING0 + (uint32_t)slot * SLOT_BYTES + (uint32_t)(c % SLOT_CHUNKS) * KCHUNK_BYTES;
+            if (c < (int)V_CHUNKS) {
+#pragma unroll
+                for (int k = 0; k < 4; ++k)
+                    mma_ts(d, tmem + TM_Q + 32u * (uint32_t)c + 8u * (uint32_t)k, sdesc_sw128(sb + 32u * k, 16u, 1024u),
+                           IDESC_S, (c > 0 || k > 0) ? 1u : 0u);
+            } else {
+#pragma unroll
+                for (int k = 0; k < 4; ++k)
+                    mma_ss(d, sdesc_sw128(smem + QPE0 + 32u * k, 16u, 1024u), sdesc_sw128(sb + 32u * k, 16u, 1024u),
+                           IDESC_S, 1u);
+            }
+            if (c % SLOT_CHUNKS == SLOT_CHUNKS - 1) mma_commit(smem_u32(&h->c_empty[slot]));
         }
-        mma_commit(smem_u32(&h->k_empty[stage]));
+        if (!ok) break;
         mma_commit(smem_u32(&h->s_full[buf]));
         mbar_arrive(smem_u32(&h->s_full[buf]));
     }
@@ -265,11 +381,14 @@ __device__ void s_role_mma(const Params &p, Header *h, uint32_t smem, uint32_t t
 }
 
 // Softmax warps 0-7 (thread = row; warp group g = warp / 4 owns keys
-// [32g, 32g + 32) of every tile).  Both groups read the full score row and
-// compute the same running maximum, so they agree on every rescale without
-// exchanging data; each exponentiates and ships only its own 32 keys.  Q goes
-// into TMEM first; after the last tile the groups add their partial sums,
-// group 0 writes the lse to the workspace and 1/l to the partner.
+// [64g, 64g + 64) of every S tile and always fills the partner's P buffer g,
+// i.e. the partner consumes an S tile as two 64-key P halves).  Pass 1 reads
+// the whole score row (the other group's half first) for the maximum, which
+// both groups therefore agree on without exchanging data; pass 2 re-reads
+// the group's own 64 scores for the exponentials.  Q goes in first: the
+// no-PE dims to TMEM, the RoPE dims to shared memory.  After the last tile
+// the groups add their partial sums; group 0 writes the lse to the
+// workspace and 1/l to the partner.
 __device__ void s_role_rows(const Params &p, Header *h, uint32_t smem, uint32_t tmem, const Unit &u)
 {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -282,11 +401,12 @@ __device__ void s_role_rows(const Params &p, Header *h, uint32_t smem, uint32_t 
     const int64_t i = row_ok ? lr / H : 0;
     const int64_t hh = row_ok ? lr % H : 0;
 
-    // Q row -> TMEM columns [0, 288): 32-bit column k/2 holds elements k, k+1.
-    // Group 0 writes dims 0..319, group 1 dims 320..575.
+    // Q row: dims 0..511 -> TMEM columns [0, 256) (32-bit column k/2 holds
+    // elements k, k+1; group 0 writes dims 0..255, group 1 dims 256..511);
+    // dims 512..575 -> shared memory, K-major 128-byte swizzled (group 1).
     const __nv_bfloat16 *qrow = p.q + (u.qo0 + i) * p.q_stride_tok + hh * p.q_stride_head;
 #pragma unroll 1
-    for (int c = grp * 5; c < (grp ? D / 64 : 5); ++c) {
+    for (int c = grp * 4; c < grp * 4 + 4; ++c) {
         uint32_t w[32];
 #pragma unroll
         for (int v = 0; v < 8; ++v) {
@@ -296,62 +416,70 @@ __device__ void s_role_rows(const Params &p, Header *h, uint32_t smem, uint32_t 
         }
         tmem_st32(tmem + lane_base + TM_Q + 32u * (uint32_t)c, w);
     }
+    if (grp == 1) {
+        uint8_t *qpe = reinterpret_cast<uint8_t *>(h) + QPE0 + (r >> 3) * 1024 + (r & 7) * 128;
+#pragma unroll
+        for (int v = 0; v < 8; ++v) {
+            uint4 x = make_uint4(0u, 0u, 0u, 0u);
+            if (row_ok) x = __ldg(reinterpret_cast<const uint4 *>(qrow + 512 + v * 8));
+            *reinterpret_cast<uint4 *>(qpe + ((v ^ (r & 7)) << 4)) = x;
+        }
+        fence_proxy_async_smem();
+    }
     tmem_st_wait();
     tc_fence_before_sync();
     named_barrier_sync(1, SOFTMAX_THREADS + 32);
 
     const int64_t mrow = p.mask_indptr[u.b] + i * u.N;
     const float sl2 = p.sm_scale * LOG2E;
-    const uint32_t peer_pbuf = map_cluster(smem + PBUF0, 1);
-    const uint32_t peer_alpha = map_cluster(smem_u32(&h->alpha[0][0]), 1);
-    const uint32_t peer_flags = map_cluster(smem_u32(&h->flags[0]), 1);
+    const uint32_t peer_pbuf = map_cluster(smem + PBUF0, 1) + (uint32_t)grp * P_BUF;
+    const uint32_t peer_alpha = map_cluster(smem_u32(&h->alpha[grp][0]), 1);
+    const uint32_t peer_flags = map_cluster(smem_u32(&h->flags[grp]), 1);
     float m_used = -INFINITY, l = 0.f;
     bool ok = true;
-    // Mask bits of tile t for this row, loaded one tile ahead.
-    auto mask_of = [&](int t) -> uint64_t {
-        const int64_t j0 = u.k0 + (int64_t)t * KEYS;
-        const int nk = (int)((u.k1 - j0) < KEYS ? (u.k1 - j0) : KEYS);
-        return (row_ok && t < u.ntiles) ? load_bits(p.custom_mask, mrow + j0, nk) : 0ull;
+    // Mask bits of S tile t for this row (two 64-bit words), loaded one tile ahead.
+    struct Bits { uint64_t w[2]; };
+    auto mask_of = [&](int t) -> Bits {
+        Bits b{{0ull, 0ull}};
+        if (row_ok && t < u.ntiles_s) {
+#pragma unroll
+            for (int hf = 0; hf < 2; ++hf) {
+                const int64_t j0 = tile_key0(u, t) + 64 * hf;
+                const int64_t nk = u.k1 - j0;
+                b.w[hf] = load_bits(p.custom_mask, mrow + j0, (int)(nk < 64 ? (nk > 0 ? nk : 0) : 64));
+            }
+        }
+        return b;
     };
-    uint64_t next_bits = mask_of(0);
+    Bits next_bits = mask_of(0);
 
-    for (int t = 0; t < u.ntiles; ++t) {
+    for (int t = 0; t < u.ntiles_s; ++t) {
         const int buf = t & 1;
-        const uint64_t bits = next_bits;
+        const Bits bits = next_bits;
         next_bits = mask_of(t + 1);
         if (!warp_wait(h, smem_u32(&h->s_full[buf]), (uint32_t)(t >> 1) & 1u, p.status, false)) { ok = false; break; }
         tc_fence_after_sync();
-        // The other group's 32 scores first (only their maximum is kept), then
-        // this group's own 32; raw scores, the scale is folded into the exponent.
-        const uint64_t vis = *reinterpret_cast<volatile uint64_t *>(&h->s_valid[buf]) & bits;
-        const uint32_t s_col = tmem + lane_base + TM_S0 + 64u * (uint32_t)buf;
-        const uint32_t v_own = (uint32_t)(vis >> (32 * grp)), v_oth = (uint32_t)(vis >> (32 * (1 - grp)));
-        const bool all_vis = __all_sync(0xffffffffu, vis == ~0ull);
+        const uint32_t s_col = tmem + lane_base + TM_S0 + 128u * (uint32_t)buf;
+        uint64_t vis[2];
+        vis[0] = *reinterpret_cast<volatile uint64_t *>(&h->s_valid[buf][0]) & bits.w[0];
+        vis[1] = *reinterpret_cast<volatile uint64_t *>(&h->s_valid[buf][1]) & bits.w[1];
+        const bool all_vis = __all_sync(0xffffffffu, (vis[0] & vis[1]) == ~0ull);
         uint32_t sv[32];
+        // pass 1: maximum over all 128 scores, the other group's half first
         float mx = -INFINITY;
-        tmem_ld32(s_col + 32u * (uint32_t)(1 - grp), sv);
-        tmem_ld_wait();
-        if (all_vis) {
 #pragma unroll
-            for (int n = 0; n < 32; ++n) mx = fmaxf(mx, __uint_as_float(sv[n]));
-        } else {
+        for (int part = 0; part < 4; ++part) {
+            const int half = (part < 2) ? 1 - grp : grp;
+            const int q = 2 * half + (part & 1);        // 32-column quarter of the row
+            tmem_ld32(s_col + 32u * (uint32_t)q, sv);
+            tmem_ld_wait();
+            const uint32_t vq = (uint32_t)(vis[half] >> (32 * (q & 1)));
+            if (all_vis) {
 #pragma unroll
-            for (int n = 0; n < 32; ++n) mx = fmaxf(mx, ((v_oth >> n) & 1u) ? __uint_as_float(sv[n]) : -INFINITY);
-        }
-        tmem_ld32(s_col + 32u * (uint32_t)grp, sv);
-        tmem_ld_wait();
-        tc_fence_before_sync();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(smem_u32(&h->s_free[buf]));
-        if (all_vis) {
+                for (int n = 0; n < 32; ++n) mx = fmaxf(mx, __uint_as_float(sv[n]));
+            } else {
 #pragma unroll
-            for (int n = 0; n < 32; ++n) mx = fmaxf(mx, __uint_as_float(sv[n]));
-        } else {
-#pragma unroll
-            for (int n = 0; n < 32; ++n) {
-                const float x = ((v_own >> n) & 1u) ? __uint_as_float(sv[n]) : -INFINITY;
-                sv[n] = __float_as_uint(x);
-                mx = fmaxf(mx, x);
+                for (int n = 0; n < 32; ++n) mx = fmaxf(mx, ((vq >> n) & 1u) ? __uint_as_float(sv[n]) : -INFINITY);
             }
         }
         mx *= sl2;                                 // maximum in log2 units (sl2 > 0 keeps the order)
@@ -363,36 +491,46 @@ __device__ void s_role_rows(const Params &p, Header *h, uint32_t smem, uint32_t 
             m_used = mx;
             rescale = true;
         }
-        if (t >= 2 && !warp_wait(h, smem_u32(&h->p_empty[buf]), (uint32_t)((t >> 1) - 1) & 1u, p.status, true)) {
+        // The partner must be done with P buffer grp (this group's half of the previous S tile).
+        if (t >= 1 && !warp_wait(h, smem_u32(&h->p_empty[grp]), (uint32_t)(t - 1) & 1u, p.status, true)) {
             ok = false;
             break;
         }
-        // p = 2^(s * sl2 - m_used); masked scores are -inf and give exactly 0.
+        // pass 2: p = 2^(s * sl2 - m_used) for this group's 64 keys; masked scores give 0.
         const float neg_m = m_used == -INFINITY ? 0.f : -m_used;
-        uint32_t pk[16];
+        const uint32_t prow = peer_pbuf + (uint32_t)(r >> 3) * 1024u + (uint32_t)(r & 7) * 128u;
         float psum = 0.f;
 #pragma unroll
-        for (int n = 0; n < 16; ++n) {
-            const float p0 = ex2_approx(fmaf(__uint_as_float(sv[2 * n]), sl2, neg_m));
-            const float p1 = ex2_approx(fmaf(__uint_as_float(sv[2 * n + 1]), sl2, neg_m));
-            psum += p0 + p1;
-            pk[n] = pack_bf16x2(p0, p1);
-        }
-        l += psum;
-        // Row r of the partner's P buffer: K-major, 128-B swizzle (A of P V);
-        // this group's 32 keys are 16-B pieces 4g .. 4g+3 of the row.
-        const uint32_t prow = peer_pbuf + (uint32_t)buf * P_BUF + (uint32_t)(r >> 3) * 1024u + (uint32_t)(r & 7) * 128u;
+        for (int part = 0; part < 2; ++part) {
+            tmem_ld32(s_col + 32u * (uint32_t)(2 * grp + part), sv);
+            tmem_ld_wait();
+            const uint32_t vq = (uint32_t)(vis[grp] >> (32 * part));
+            uint32_t pk[16];
 #pragma unroll
-        for (int q = 0; q < 4; ++q)
-            st_cluster_v4(prow + ((((uint32_t)(4 * grp + q)) ^ (uint32_t)(r & 7)) << 4), pk[4 * q], pk[4 * q + 1],
-                          pk[4 * q + 2], pk[4 * q + 3]);
-        if (grp == 0) {
-            st_cluster_f32(peer_alpha + (uint32_t)(buf * ROWS + r) * 4u, rescale ? alpha : 1.f);
-            const uint32_t any = __any_sync(0xffffffffu, rescale) ? 1u : 0u;
-            if (lane == 0) st_cluster_u8(peer_flags + (uint32_t)buf * 4u + (uint32_t)quad, any);
+            for (int n = 0; n < 16; ++n) {
+                const float a0 = (all_vis || ((vq >> (2 * n)) & 1u)) ? __uint_as_float(sv[2 * n]) : -INFINITY;
+                const float a1 = (all_vis || ((vq >> (2 * n + 1)) & 1u)) ? __uint_as_float(sv[2 * n + 1]) : -INFINITY;
+                const float p0 = ex2_approx(fmaf(a0, sl2, neg_m));
+                const float p1 = ex2_approx(fmaf(a1, sl2, neg_m));
+                psum += p0 + p1;
+                pk[n] = pack_bf16x2(p0, p1);
+            }
+            // keys 32*part .. 32*part+31 of this group's half: 16-B pieces 4*part .. 4*part+3 of row r
+#pragma unroll
+            for (int qq = 0; qq < 4; ++qq)
+                st_cluster_v4(prow + ((((uint32_t)(4 * part + qq)) ^ (uint32_t)(r & 7)) << 4), pk[4 * qq],
+                              pk[4 * qq + 1], pk[4 * qq + 2], pk[4 * qq + 3]);
         }
+        tc_fence_before_sync();
         __syncwarp();
-        if (lane == 0) mbar_arrive(smem_u32(&h->p_written[buf]));
+        if (lane == 0) mbar_arrive(smem_u32(&h->s_free[buf]));
+        l += psum;
+        // The O tile of group 0's half rescales O first; group 1's half follows with the same maximum.
+        st_cluster_f32(peer_alpha + (uint32_t)r * 4u, (grp == 0 && rescale) ? alpha : 1.f);
+        const uint32_t any = (grp == 0 && __any_sync(0xffffffffu, rescale)) ? 1u : 0u;
+        if (lane == 0) st_cluster_u8(peer_flags + (uint32_t)quad, any);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&h->p_written[grp]));
     }
 
     // Partial sums of group 1 -> group 0 (both groups always reach this barrier).
@@ -411,10 +549,10 @@ __device__ void s_role_rows(const Params &p, Header *h, uint32_t smem, uint32_t 
     if (lane == 0) mbar_arrive_cluster(smem_u32(&h->l_ready), 1);
 }
 
-// Sender (warp 17, lane 0): once all 8 softmax warps stored a P tile into the
+// Sender (warp 17, lane 0): once a softmax group stored its P half into the
 // partner, order those writes for the partner's tensor-core reads and
-// publish the tile.  Keeps the proxy fence and the cluster-scope release off
-// the softmax warps.
+// publish the O tile.  Keeps the proxy fence and the cluster-scope release
+// off the softmax warps.
 __device__ void s_role_sender(const Params &p, Header *h, const Unit &u)
 {
     for (int t = 0; t < u.ntiles; ++t) {
@@ -557,19 +695,26 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
     u.k0 = (int64_t)u.split * chunk;
     if (u.k0 >= u.N) return;
     u.k1 = (u.k0 + chunk < u.N) ? u.k0 + chunk : u.N;
-    u.ntiles = (int)((u.k1 - u.k0 + KEYS - 1) / KEYS);
+    u.ntiles_s = (int)((u.k1 - u.k0 + KEYS_S - 1) / KEYS_S);
+    u.ntiles = 2 * u.ntiles_s;
+    {
+        const int64_t row_tiles = (u.rows_b + ROWS - 1) / ROWS;
+        u.rot = (int)(((int64_t)(blockIdx.x >> 1) * u.ntiles_s) / row_tiles);
+    }
 
     if (tid == 0) {
+        for (int s = 0; s < NSLOT; ++s) {
+            mbar_init(smem_u32(&h->c_full[s]), PRODUCER_WARPS);
+            mbar_init(smem_u32(&h->c_empty[s]), 1);
+        }
         for (int s = 0; s < STAGES; ++s) {
-            mbar_init(smem_u32(&h->k_full[s]), PRODUCER_WARPS);
-            mbar_init(smem_u32(&h->k_empty[s]), 1);
             mbar_init(smem_u32(&h->v_full[s]), PRODUCER_WARPS);
             mbar_init(smem_u32(&h->v_empty[s]), 1);
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(smem_u32(&h->s_full[i]), 2);
             mbar_init(smem_u32(&h->s_free[i]), SOFTMAX_THREADS / 32);
-            mbar_init(smem_u32(&h->p_written[i]), SOFTMAX_THREADS / 32);
+            mbar_init(smem_u32(&h->p_written[i]), SOFTMAX_THREADS / 64);
             mbar_init(smem_u32(&h->p_empty[i]), 1 + 4);
             mbar_init(smem_u32(&h->p_full[i]), 1);
             h->flags[i] = 0u;
@@ -597,7 +742,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
         if (warp < PRODUCER_WARP0) {
             s_role_rows(p, h, smem, tmem, u);
         } else if (warp < MMA_WARP) {
-            gather_tiles<K_CHUNKS>(p, h, &pool_map, smem + STAGE0, K_STAGE, h->k_full, h->k_empty, h->k_valid, u);
+            s_role_gather(p, h, &pool_map, smem, u);
         } else if (warp == MMA_WARP) {
             named_barrier_sync(1, SOFTMAX_THREADS + 32);
             tc_fence_after_sync();

@@ -12,7 +12,7 @@ import math
 from typing import Sequence
 
 NUM_SMS = 152                  # GB300: 2 dies x 76 SMs
-KEY_ALIGN = 64                 # must match the library's split chunk rule
+KEY_ALIGN = 128                # must match the library's split chunk rule
 MIN_CHUNK = 256
 CANDIDATES = (1, 2, 3, 4, 5, 6, 7, 8, 10, 12, 14, 16, 20, 24, 28, 32, 40, 48, 56, 64, 80, 96, 128, 160, 192, 256)
 
