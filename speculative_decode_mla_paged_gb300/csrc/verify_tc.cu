@@ -1,4 +1,5 @@
-// Tensor-core split kernel for tree-verify attention (sm_103a: tcgen05, TMEM).
+// Tensor-core split kernel for tree-verify attention (sm_103a: tcgen05, TMEM,
+// TMA gathers, bulk copies between the CTAs of a cluster).
 //
 // Work unit: one (key split, 128-row tile, request), the same unit as the
 // pages' split-KV flash-decode partial ("The Capture-Safe Kernel",
@@ -7,35 +8,45 @@
 // Chasm", section Decision) and both contractions run on the tensor cores.
 //
 // Why a 2-CTA cluster per unit.  A 128 x 512 fp32 output accumulator is the
-// whole of an SM's TMEM (128 lanes x 512 columns), and a 128 x 576 bf16 Q
-// tile is 144 KB of shared memory, so one SM cannot hold Q, the scores S
-// and O for 128 rows while feeding M = 128 MMAs at full rate.  The pair
-// splits the work by role:
+// whole of an SM's TMEM (128 lanes x 512 columns), so one SM cannot hold Q,
+// the scores S and O for 128 rows.  The pair splits the work by role:
 //
-//   CTA rank 0 ("S"): Q lives in TMEM (288 columns of packed bf16, the A
-//     operand of S = Q K^T from tensor memory); K tiles (64 keys x 576) are
-//     gathered into shared memory; two 64-column S buffers in TMEM.  Its
-//     four row warps (thread = row) read S, apply the packed tree mask, run
-//     the online softmax and write P (bf16) straight into the partner's
-//     shared memory.
-//   CTA rank 1 ("O"): the 128 x 512 fp32 O accumulator fills its TMEM;
-//     V tiles (64 keys x 512, the first 512 dims of the same rows) are
-//     gathered into shared memory; O += P V on the tensor cores.
+//   CTA rank 0 ("S"): Q's 512 no-PE dims live in TMEM (256 columns of packed
+//     bf16, the A operand of S = Q K^T from tensor memory), its 64 RoPE dims
+//     in shared memory; a 128-key tile of K arrives by TMA gather4 as three
+//     rounds of three 16 KB column chunks (a ring of one tile); two
+//     128-column S buffers in TMEM.  Eight softmax warps (two groups of four,
+//     thread = row, group g owns keys [64g, 64g + 64) of each tile) read
+//     their scores once, exchange the row maximum through shared memory,
+//     write P (bf16) to a local staging slot and ship each 64-key half to
+//     the partner with one bulk copy whose bytes complete the partner's
+//     barrier.
+//   CTA rank 1 ("O"): the fp32 O accumulator fills its TMEM; V (the first
+//     512 dims of the same rows) arrives by TMA gather4 in 64-key x 256-dim
+//     half tiles; P halves land in four double-buffered slots;
+//     O += P V runs as N = 256 MMAs with both operands in shared memory.
 //
-// Per 64-key tile the S CTA issues 36 MMAs (M128 N64 K16, A from TMEM) and
-// the O CTA 8 (M128 N256 K16, both operands in shared memory), so the two
-// SMs carry 576 and 512 MACs per (row, key): balanced.
+// Per 128-key tile the S CTA issues 36 MMAs (M128 N128 K16) and the O CTA 16
+// (M128 N256 K16): 576 and 512 MACs per (row, key), balanced.
 //
-// Online softmax uses a lazy maximum: O is rescaled only when a row's
-// running maximum grows by more than 2^8 (log2 units), so P stays <= 256;
-// the S CTA sends the per-row factor and a per-warp flag with each P tile
-// and the O CTA's row warps rescale their TMEM rows only on flagged tiles.
+// Gathers are the throughput limit of this design (a TMA gather4 moves
+// 512 B, and one warp issues them one at a time, lane after lane), so each
+// CTA runs 16 producer warps in two teams that take turns round by round,
+// and setmaxnreg moves registers from the producer warpgroups to the
+// softmax / row warpgroups.
 //
-// Each thread role, the barriers between them, and the shared-memory
-// layouts (128-byte swizzle; one gathered tile serves as K-major B of
-// Q K^T and as MN-major B of P V) are described where they are defined.
-// Every wait is bounded (1 s of global time): on expiry the kernel sets
-// STATUS_TIMEOUT, unwinds, drains its MMAs and frees TMEM.
+// Online softmax with a lazy maximum: O is rescaled only when a row's
+// running maximum grows by more than 2^8 (log2 units), so P stays <= 256.
+// The P transfer of a tile's first half carries the per-row factor and a
+// per-warp flag; the O CTA's row warps rescale their TMEM rows only when a
+// flag is set.
+//
+// Synchronisation uses mbarriers only: TMA and bulk-copy bytes complete
+// barriers directly, tensor-core commits arrive on them (across the pair
+// with a multicast commit), and no cluster-scope release is on the per-tile
+// path.  Every wait is bounded (1 s of global time): on expiry the kernel
+// sets STATUS_TIMEOUT, unwinds, lets the copies it issued land, drains its
+// MMAs and frees TMEM.
 #include "va_internal.cuh"
 #include "tc_ptx.cuh"
 
@@ -50,38 +61,47 @@ namespace {
 using namespace ptx;
 
 constexpr int ROWS = 128;                  // rows per unit = M of every MMA
-constexpr int KEYS = 64;                   // keys per O-role tile (one P half)
-constexpr int KEYS_S = 128;                // keys per S-role tile (N of the score MMAs)
-constexpr int STAGES = 3;                  // O role: gathered V tiles in flight
-constexpr int NSLOT = 4;                   // S role: ring of 48 KB slots, 3 K chunks (128 keys x 64 dims) each
-constexpr int SLOT_CHUNKS = 3;
-constexpr int THREADS = 576;               // warps 0-7 rows, 8-15 gather (TMA), 16 MMA issue, 17 P sender
-constexpr int SOFTMAX_THREADS = 256;       // S role: two warp groups, each owns half the keys of a tile
-constexpr int PRODUCER_WARP0 = 8;          // TMA issue is serial within a warp, so 8 warps share it
-constexpr int PRODUCER_WARPS = 8;
-constexpr int MMA_WARP = 16;
-constexpr int SENDER_WARP = 17;
-constexpr uint32_t CHUNK_BYTES = KEYS * 128;          // one 64-dim column block of a tile
-constexpr uint32_t K_CHUNKS = D / 64;                 // 9
-constexpr uint32_t V_CHUNKS = DV / 64;                // 8
-constexpr uint32_t KCHUNK_BYTES = KEYS_S * 128;       // 16384: one K chunk of an S tile
-constexpr uint32_t SLOT_BYTES = SLOT_CHUNKS * KCHUNK_BYTES;
-constexpr uint32_t V_STAGE = V_CHUNKS * CHUNK_BYTES;  // 65536
-constexpr uint32_t P_BUF = ROWS * KEYS * 2;           // 16384
+constexpr int KEYS_S = 128;                // keys per S tile (N of the score MMAs)
+constexpr int KEYS_O = 64;                 // keys per O tile (one P half)
+constexpr int THREADS = 896;               // 28 warps = 7 warpgroups
+constexpr int SOFTMAX_THREADS = 256;       // S: warps 0-7 (warpgroups 0, 1)
+constexpr int PRODUCER_WARP0 = 8;          // both: warps 8-23 (warpgroups 2-5) issue the TMA gathers,
+constexpr int TEAM_WARPS = 8;              //   two teams of 8 warps taking turns by round
+constexpr int MMA_WARP = 24;               // both: warpgroup 6; lane 0 of warp 24 issues the MMAs
+constexpr int LAUNCH_REGS = 72;            // registers per thread at launch: 65536 / 896, rounded down to 8
+constexpr int REGS_WIDE = 128;             // softmax and O-row warpgroups after setmaxnreg
+constexpr int REGS_NARROW = 48;            // producer, MMA and idle warpgroups
+static_assert(8 * 32 * REGS_WIDE + 20 * 32 * REGS_NARROW <= THREADS * LAUNCH_REGS,
+              "the register split fits the launch allocation");
+constexpr uint32_t K_CHUNKS = D / 64;      // 9 column chunks per S tile
+constexpr uint32_t KCHUNK = KEYS_S * 128;  // 16 KB: 128 keys x 64 dims
+constexpr int RCHUNKS = 3;                 // S: chunks per gather round
+constexpr uint32_t KROUND = RCHUNKS * KCHUNK;   // 48 KB
+constexpr int NKR = K_CHUNKS / RCHUNKS;    // S: ring of 3 rounds (one tile); round g of every tile uses slot g
+constexpr uint32_t VCHUNK = KEYS_O * 128;  // 8 KB: 64 keys x 64 dims
+constexpr uint32_t VHALF = 4 * VCHUNK;     // 32 KB: 64 keys x 256 dims, the B of one N = 256 MMA
+constexpr int NVH = 4;                     // O: V half-tile ring
+constexpr uint32_t PTILE = ROWS * KEYS_O * 2;   // 16 KB P half: 128 rows x 64 keys bf16
+constexpr uint32_t SIDE_BYTES = ROWS * 4 + 16;  // alpha[128] + 4 warp flags, after P in a first-half slot
+constexpr uint32_t PSLOT = PTILE + 1024;        // 17 KB (keeps every slot 1 KB aligned)
 constexpr uint32_t HEADER = 2048;
-constexpr uint32_t STAGE0 = HEADER;                   // both roles: gathered tiles
-constexpr uint32_t PBUF0 = HEADER + STAGES * V_STAGE; // O role: two P buffers
-constexpr uint32_t SMEM_USED = PBUF0 + 2 * P_BUF;
-constexpr uint32_t SMEM_ALLOC = SMEM_USED + 1024;     // room to align the base to 1 KB
-constexpr uint32_t QPE0 = HEADER;                     // S role: Q's 64 RoPE dims, 128 x 128 B (A of 4 MMAs)
-constexpr uint32_t RING0 = QPE0 + ROWS * 128;         // S role: K chunk ring
-constexpr uint32_t S_SCRATCH = RING0 + NSLOT * SLOT_BYTES; // S role: per-row partial sums of the 2nd group
-static_assert(S_SCRATCH + ROWS * 4 <= SMEM_USED, "S role layout");
+// S CTA shared memory
+constexpr uint32_t S_QPE = HEADER;                   // Q RoPE dims: 128 rows x 128 B, A of the 4 last MMAs
+constexpr uint32_t S_STAGE = S_QPE + ROWS * 128;     // P staging, one slot per softmax group
+constexpr uint32_t S_RING = S_STAGE + 2 * PSLOT;     // K round ring
+constexpr uint32_t S_XMAX = S_RING + NKR * KROUND;   // row maxima exchanged by the two groups [tile parity][group][row]
+constexpr uint32_t S_END = S_XMAX + 2 * 2 * ROWS * 4;
+// O CTA shared memory
+constexpr uint32_t O_PSLOT = HEADER;                 // P slots [group][tile parity]
+constexpr uint32_t O_VRING = O_PSLOT + 4 * PSLOT;    // V half-tile ring
+constexpr uint32_t O_END = O_VRING + NVH * VHALF;
+constexpr uint32_t SMEM_USED = S_END > O_END ? S_END : O_END;
+constexpr uint32_t SMEM_ALLOC = SMEM_USED + 1024;    // room to align the base to 1 KB
 static_assert(SMEM_ALLOC <= 232448, "at most 227 KB of shared memory per CTA");
+static_assert(S_RING % 1024 == 0 && O_VRING % 1024 == 0 && PSLOT % 1024 == 0, "swizzle atoms are 1 KB aligned");
 
 constexpr uint32_t TMEM_COLS = 512;
-constexpr uint32_t TM_Q = 0;                          // S role: Q's 512 no-PE dims, 256 columns
-constexpr uint32_t TM_S0 = 256;                       // S role: S buffers at 256 and 384 (128 columns each)
+constexpr uint32_t TM_S0 = 256;                      // S role: S buffers at columns 256 and 384
 constexpr uint32_t IDESC_S = idesc_bf16(128, 128, false);
 constexpr uint32_t IDESC_PV = idesc_bf16(128, 256, true);
 constexpr float LOG2E = 1.4426950408889634f;
@@ -92,285 +112,242 @@ constexpr uint64_t TIMEOUT_NS = 1000000000ull;
 // Shared-memory header at the (1 KB aligned) base; same offsets in both CTAs
 // so a barrier or field can be addressed in the partner with mapa.
 struct Header {
-    uint64_t c_full[NSLOT];    // S: 3 K chunks landed in a ring slot (8 producer-warp arrives + TMA bytes)
-    uint64_t c_empty[NSLOT];   // S: MMAs reading the slot completed (commit)
-    uint64_t s_full[2];        // S: scores ready (commit) + valid-key bits published (MMA thread)
+    uint64_t c_full[NKR];      // S: K round landed (8 producer-warp arrives + TMA bytes)
+    uint64_t c_empty[NKR];     // S: the MMAs reading the round completed (commit)
+    uint64_t s_full[2];        // S: scores ready (commit) + valid-key bits copied (MMA thread)
     uint64_t s_free[2];        // S: the 8 softmax warps have read the score buffer
-    uint64_t p_written[2];     // S: softmax group g (4 warps) stored its P half into the partner's buffer g
-    uint64_t p_empty[2];       // S: partner done with a P buffer (its commit + its 4 row-warp leaders)
-    uint64_t v_full[STAGES];   // O: gathered V tile landed (8 producer-warp arrives + TMA bytes)
-    uint64_t v_empty[STAGES];  // O: MMAs reading the stage completed
-    uint64_t p_full[2];        // O: partner's sender warp published a P tile
+    uint64_t p_empty[2][2];    // S: the partner's P V MMAs on P slot [group][parity] completed (its commit)
+    uint64_t v_full[NVH];      // O: V half tile landed (8 producer-warp arrives + TMA bytes)
+    uint64_t v_empty[NVH];     // O: the MMAs reading it completed
+    uint64_t p_full[2][2];     // O: P slot landed (the MMA thread's expect-tx arrive + bulk-copy bytes)
     uint64_t pv_sync;          // O: every MMA issued so far completed (before a rescale)
-    uint64_t rs_req;           // O: MMA thread asks the row warps to rescale O
-    uint64_t rs_done;          // O: 128 row threads rescaled their rows
-    uint64_t l_ready;          // O: partner's 4 row warps wrote 1/l
+    uint64_t rs_req;           // O: MMA thread asks the row warps to rescale O (or to finish)
+    uint64_t rs_done;          // O: the 4 row warps rescaled their rows
+    uint64_t l_ready;          // O: the partner's 4 group-0 warps wrote 1/l
     uint64_t drain;            // both: all MMAs of the CTA completed
     uint64_t t_valid[2][2];    // S: bit n of an S tile's 128 keys = key n has a valid slot (tile ring of 2)
     uint64_t s_valid[2][2];    // S: the same bits, per score buffer
     uint32_t tmem_base;
     uint32_t abort;
-    uint32_t flags[2];         // O: byte w != 0 if a row of warp w rescales on this P buffer
-    float alpha[2][ROWS];      // O: per-row rescale factor for the tile in each P buffer
+    int32_t rs_slot;           // O: tile parity of the P slot whose factors to apply; -1: finish
+    uint32_t pad;
     float inv_l[ROWS];         // O: 1 / softmax denominator per row (0 if the row saw nothing)
+    float lpart[ROWS];         // S: group 1's partial sums
 };
 static_assert(sizeof(Header) <= HEADER, "header fits");
 
 struct Unit {
     int split, b;
     int64_t qo0, kv0, L, N, k0, k1, r0, rows_b;
-    int ntiles_s;              // S tiles of 128 keys
-    int ntiles;                // O tiles of 64 keys = 2 * ntiles_s (the last may be empty)
+    int ntiles;                // S tiles of 128 keys; the O CTA processes 2 * ntiles 64-key halves
     int rot;                   // this pair starts at S tile `rot` of its split (see tile_key0)
 };
 
 // First key of the t-th S tile this pair processes.  The row tiles of one
 // request read the same keys; each starts at a different tile of the split
-// (rot = row tile * ntiles_s / row tiles) so they do not request the same
-// rows from L2 at the same moment.  Softmax order does not change the result.
+// (rot = row tile * ntiles / row tiles) so they do not request the same rows
+// from L2 at the same moment.  Softmax order does not change the result.
 __device__ __forceinline__ int64_t tile_key0(const Unit &u, int t)
 {
     int s = t + u.rot;
-    if (s >= u.ntiles_s) s -= u.ntiles_s;
+    if (s >= u.ntiles) s -= u.ntiles;
     return u.k0 + (int64_t)s * KEYS_S;
 }
 
-// First key of the u-th O tile (64 keys: the two halves of each S tile).
-__device__ __forceinline__ int64_t otile_key0(const Unit &u, int t)
-{
-    return tile_key0(u, t >> 1) + (int64_t)(t & 1) * KEYS;
-}
+// ------------------------------------------------------------------ bounded waits
 
-// Bounded wait on phase `parity` of a barrier.  False after a timeout (status
-// bit set, abort flag raised) or when another thread of the CTA aborted.
-__device__ __noinline__ bool wait_bar(Header *h, uint32_t bar, uint32_t parity, unsigned *status, bool cluster,
-                                      bool stop_on_abort = true)
+__device__ __forceinline__ bool wait_slow(Header *h, uint32_t bar, uint32_t parity, unsigned *status, bool cluster,
+                                       bool stop_on_abort)
 {
-    if (cluster ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = globaltimer_ns();
     for (uint32_t it = 1;; ++it) {
         if (cluster ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity)) return true;
         if ((it & 63u) == 0) {
             if (stop_on_abort && *reinterpret_cast<volatile uint32_t *>(&h->abort)) return false;
             if (globaltimer_ns() - t0 > TIMEOUT_NS) {
-                atomicOr(status, STATUS_TIMEOUT);
-                *reinterpret_cast<volatile uint32_t *>(&h->abort) = 1u;
+                if (stop_on_abort) {
+                    atomicOr(status, STATUS_TIMEOUT);
+                    *reinterpret_cast<volatile uint32_t *>(&h->abort) = 1u;
+                }
                 return false;
             }
         }
     }
 }
 
-// The same for all 32 lanes of a warp: true only if every lane's wait succeeded
-// (keeps the warp converged for the .sync.aligned tcgen05 instructions).
-__device__ __forceinline__ bool warp_wait(Header *h, uint32_t bar, uint32_t parity, unsigned *status, bool cluster)
+// Wait for phase `parity` of a barrier.  False after a timeout (status bit
+// set, abort flag raised) or when another thread of the CTA aborted.
+__device__ __forceinline__ bool wait_bar(Header *h, uint32_t bar, uint32_t parity, unsigned *status,
+                                         bool cluster = false, bool stop_on_abort = true)
+{
+    if (cluster ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity)) return true;
+    return wait_slow(h, bar, parity, status, cluster, stop_on_abort);
+}
+
+// The same for all 32 lanes of a warp (keeps the warp converged for the
+// .sync.aligned tcgen05 instructions that follow).
+__device__ __forceinline__ bool warp_wait(Header *h, uint32_t bar, uint32_t parity, unsigned *status,
+                                          bool cluster = false)
 {
     return __all_sync(0xffffffffu, wait_bar(h, bar, parity, status, cluster)) != 0;
 }
 
-// nbits (<= 64) mask bits starting at bit index bit0, bit n of the result =
-// bit bit0 + n; bytes are read only inside that range.
-__device__ __forceinline__ uint64_t load_bits(const uint8_t *mask, int64_t bit0, int nbits)
+// After a timeout: TMA gathers and bulk copies already issued into this
+// CTA's shared memory finish within microseconds; wait 50 us before the
+// CTA may exit so none lands in memory that is no longer this CTA's.
+__device__ __forceinline__ void settle_copies()
 {
-    if (nbits <= 0) return 0ull;
-    const int64_t first = bit0 >> 3, last = (bit0 + nbits - 1) >> 3;
-    const int nb = (int)(last - first + 1);
-    uint64_t lo = 0, hi = 0;
-#pragma unroll
-    for (int k = 0; k < 9; ++k) {
-        if (k < nb) {
-            const uint64_t v = __ldg(mask + first + k);
-            if (k < 8) lo |= v << (8 * k); else hi = v;
-        }
-    }
-    const int sh = (int)(bit0 & 7);
-    uint64_t w = sh ? ((lo >> sh) | (hi << (64 - sh))) : lo;
-    if (nbits < 64) w &= (1ull << nbits) - 1ull;
-    return w;
-}
-
-// ------------------------------------------------------------------ gather (warps 8-15, both roles)
-//
-// Tile layout in shared memory: NCH column blocks of 64 dims; block c holds
-// the 64 keys as 128-B rows (key n at n*128), 16-B pieces swizzled as
-// piece q -> q ^ (n & 7) inside each 1 KB group of 8 keys (the tensor map's
-// 128-byte swizzle).  Read as B of Q K^T it is K-major (rows = keys); read as
-// B of P V it is MN-major (64 contiguous dims per key row, 8 keys per 1 KB
-// group).  Producer warp w (0..7) owns keys 8w..8w+7: lanes 0 and 1 each
-// gather four keys with one TMA gather4 per column block (a warp issues its
-// TMA instructions one after another, so the tile is spread over 8 warps).
-// A key without a valid slot reads row pool_size, outside the map, which
-// TMA fills with zeros.  Slots are loaded two tiles ahead, without branches
-// on the loaded values, so the index loads overlap the stage waits.
-template <int NCH>
-__device__ void gather_tiles(const Params &p, Header *h, const CUtensorMap *tmap, uint32_t stage_base,
-                             uint32_t stage_bytes, uint64_t *full, uint64_t *empty, uint64_t *valid, const Unit &u)
-{
-    const int pw = (int)(threadIdx.x >> 5) - PRODUCER_WARP0;
-    const int lane = threadIdx.x & 31;
-    const int64_t oob = p.pool_size;
-    struct Rows { int64_t s[4]; };
-    // Raw slots of this lane's 4 keys of tile t (-1 past the split or for idle lanes).
-    auto load_rows = [&](int t) -> Rows {
-        Rows r;
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-            const int64_t j = (t < u.ntiles ? otile_key0(u, t) : 0) + pw * 8 + lane * 4 + k;
-            const bool live = lane < 2 && t < u.ntiles && j < u.k1;
-            int64_t s = -1;
-            if (live) {
-                if (j < u.L) s = p.kv_indices ? (int64_t)__ldg(p.kv_indices + u.kv0 + j) : -2;
-                else s = p.out_cache_loc ? __ldg(p.out_cache_loc + u.qo0 + (j - u.L)) : -2;
-                if (s < 0 || s >= oob) s = -2;          // invalid slot: flagged, read as zeros
-            }
-            r.s[k] = s;
-        }
-        return r;
-    };
-    Rows ahead1 = load_rows(0), ahead2 = load_rows(1);
-    for (int t = 0; t < u.ntiles; ++t) {
-        const int stage = t % STAGES;
-        const Rows cur = ahead1;
-        ahead1 = ahead2;
-        ahead2 = load_rows(t + 2);
-        if (t >= STAGES &&
-            !__all_sync(0xffffffffu, wait_bar(h, smem_u32(&empty[stage]), (uint32_t)((t / STAGES) - 1) & 1u, p.status, false)))
-            break;
-        uint32_t nib = 0, bad = 0;
-        int y[4];
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-            nib |= (cur.s[k] >= 0 ? 1u : 0u) << k;
-            bad |= cur.s[k] == -2 ? 1u : 0u;
-            y[k] = cur.s[k] >= 0 ? (int)cur.s[k] : (int)oob;
-        }
-        if (bad) atomicOr(p.status, STATUS_BAD_SLOT);
-        const uint32_t nib1 = __shfl_sync(0xffffffffu, nib, 1);
-        const uint32_t bar = smem_u32(&full[stage]);
-        if (lane == 0) {
-            if (valid != nullptr)
-                reinterpret_cast<volatile uint8_t *>(&valid[stage])[pw] = (uint8_t)(nib | (nib1 << 4));
-            if (pw == 0) mbar_arrive_expect_tx(bar, NCH * CHUNK_BYTES);
-            else mbar_arrive(bar);
-        }
-        if (lane < 2) {
-            const uint32_t dst = stage_base + (uint32_t)stage * stage_bytes + (uint32_t)(pw * 2 + lane) * 512u;
-#pragma unroll
-            for (int c = 0; c < NCH; ++c) tma_gather4(dst + c * CHUNK_BYTES, tmap, c * 64, y[0], y[1], y[2], y[3], bar);
-        }
+    const uint64_t t0 = globaltimer_ns();
+    while (globaltimer_ns() - t0 < 50000ull) {
     }
 }
 
-// ------------------------------------------------------------------ S role
-//
-// An S tile is 128 keys.  Its K rows reach shared memory as nine 16 KB
-// chunks (128 keys x 64 dims, same 128-byte swizzled key-row layout as the
-// V tiles), three chunks per slot of a 4-slot ring with one barrier pair per
-// slot, so the score MMAs (N = 128, the shape that runs at full tensor rate)
-// can start on a tile's first chunks while its later chunks are in flight.
+// ------------------------------------------------------------------ slots of four keys
 
-// Gather (warps 8-15): producer warp w owns keys 16w..16w+15 of each S tile;
-// lanes 0-3 each gather four keys, one TMA gather4 per chunk.
-__device__ void s_role_gather(const Params &p, Header *h, const CUtensorMap *tmap, uint32_t smem, const Unit &u)
+// Raw slots of keys j0..j0+3 of the unit's request; bit k of `live` = key
+// j0+k is inside the split.  Loads are issued here and used a tile later.
+struct RawSlots {
+    int64_t s[4];
+    uint32_t live;
+};
+
+__device__ __forceinline__ RawSlots load_slots(const Params &p, const Unit &u, int64_t j0, bool lane_active)
 {
-    const int pw = (int)(threadIdx.x >> 5) - PRODUCER_WARP0;
+    RawSlots r;
+    r.live = 0;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        const int64_t j = j0 + k;
+        r.s[k] = -1;
+        if (lane_active && j < u.k1) {
+            r.live |= 1u << k;
+            if (j < u.L) r.s[k] = p.kv_indices ? (int64_t)__ldg(p.kv_indices + u.kv0 + j) : -1;
+            else r.s[k] = p.out_cache_loc ? __ldg(p.out_cache_loc + u.qo0 + (j - u.L)) : -1;
+        }
+    }
+    return r;
+}
+
+// Gather rows of the four keys (a key without a valid slot reads row
+// pool_size, outside the tensor map, which TMA fills with zeros) and the
+// valid-bit nibble; a live key with an invalid slot raises STATUS_BAD_SLOT.
+struct Slots {
+    int y[4];
+    uint32_t nib;
+};
+
+__device__ __forceinline__ Slots resolve_slots(const Params &p, const RawSlots &r)
+{
+    Slots o;
+    o.nib = 0;
+    bool bad = false;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        const bool ok = r.s[k] >= 0 && r.s[k] < p.pool_size;
+        o.y[k] = ok ? (int)r.s[k] : (int)p.pool_size;
+        o.nib |= (ok ? 1u : 0u) << k;
+        bad |= ((r.live >> k) & 1u) && !ok;
+    }
+    if (bad) atomicOr(p.status, STATUS_BAD_SLOT);
+    return o;
+}
+
+// ------------------------------------------------------------------ S role: gather (warps 8-23)
+//
+// K chunk layout: 128 keys as 128-B rows (key n at n*128) of one 64-dim
+// column block, 16-B pieces swizzled q -> q ^ (n & 7) inside each 1 KB group
+// of 8 keys (the tensor map's 128-byte swizzle): the K-major B operand of
+// the score MMAs.  A tile arrives as three rounds of three chunks; round g
+// of tile t goes to ring slot g and is issued by team (t + g) & 1.  Team
+// warp w owns keys 16w..16w+15 of each tile: lanes 0-3 each gather four
+// keys, one TMA gather4 per chunk of the round.  Both teams resolve the
+// slots of every tile.
+__device__ void s_gather(const Params &p, Header *h, const CUtensorMap *tmap, uint32_t smem, const Unit &u)
+{
+    const int pwa = (int)(threadIdx.x >> 5) - PRODUCER_WARP0;
+    const int team = pwa / TEAM_WARPS, pw = pwa % TEAM_WARPS;
     const int lane = threadIdx.x & 31;
-    const int64_t oob = p.pool_size;
-    struct Rows { int64_t s[4]; };
-    auto load_rows = [&](int t) -> Rows {
-        Rows r;
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-            const int64_t j = (t < u.ntiles_s ? tile_key0(u, t) : 0) + pw * 16 + lane * 4 + k;
-            const bool live = lane < 4 && t < u.ntiles_s && j < u.k1;
-            int64_t s = -1;
-            if (live) {
-                if (j < u.L) s = p.kv_indices ? (int64_t)__ldg(p.kv_indices + u.kv0 + j) : -2;
-                else s = p.out_cache_loc ? __ldg(p.out_cache_loc + u.qo0 + (j - u.L)) : -2;
-                if (s < 0 || s >= oob) s = -2;          // invalid slot: flagged, read as zeros
-            }
-            r.s[k] = s;
-        }
-        return r;
-    };
-    Rows ahead1 = load_rows(0), ahead2 = load_rows(1);
-    for (int t = 0; t < u.ntiles_s; ++t) {
-        const Rows cur = ahead1;
-        ahead1 = ahead2;
-        ahead2 = load_rows(t + 2);
-        uint32_t nib = 0, bad = 0;
-        int y[4];
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-            nib |= (cur.s[k] >= 0 ? 1u : 0u) << k;
-            bad |= cur.s[k] == -2 ? 1u : 0u;
-            y[k] = cur.s[k] >= 0 ? (int)cur.s[k] : (int)oob;
-        }
-        if (bad) atomicOr(p.status, STATUS_BAD_SLOT);
+    const bool act = lane < 4;
+    const int koff = pw * 16 + lane * 4;
+    RawSlots raw = load_slots(p, u, tile_key0(u, 0) + koff, act);
+    Slots cur = resolve_slots(p, raw);
+    if (u.ntiles > 1) raw = load_slots(p, u, tile_key0(u, 1) + koff, act);
+    bool ok = true;
+    for (int t = 0; t < u.ntiles && ok; ++t) {
         uint32_t bits16 = 0;
 #pragma unroll
-        for (int l = 0; l < 4; ++l) bits16 |= __shfl_sync(0xffffffffu, nib, l) << (4 * l);
-        bool ok = true;
-        for (int gi = 0; gi < (int)K_CHUNKS / SLOT_CHUNKS; ++gi) {
-            const int q = t * ((int)K_CHUNKS / SLOT_CHUNKS) + gi, slot = q % NSLOT, use = q / NSLOT;
-            if (use > 0 &&
-                !__all_sync(0xffffffffu, wait_bar(h, smem_u32(&h->c_empty[slot]), (uint32_t)(use - 1) & 1u, p.status, false))) {
+        for (int l = 0; l < 4; ++l) bits16 |= __shfl_sync(0xffffffffu, cur.nib, l) << (4 * l);
+#pragma unroll
+        for (int g = 0; g < NKR; ++g) {
+            if (((t + g) & 1) != team) continue;
+            if (t > 0 && !__all_sync(0xffffffffu, wait_bar(h, smem_u32(&h->c_empty[g]), (uint32_t)(t - 1) & 1u, p.status))) {
                 ok = false;
                 break;
             }
-            const uint32_t bar = smem_u32(&h->c_full[slot]);
+            const uint32_t bar = smem_u32(&h->c_full[g]);
             if (lane == 0) {
-                if (gi == 0) reinterpret_cast<volatile uint16_t *>(&h->t_valid[t & 1][0])[pw] = (uint16_t)bits16;
-                if (pw == 0) mbar_arrive_expect_tx(bar, SLOT_BYTES);
+                if (g == 0) reinterpret_cast<volatile uint16_t *>(&h->t_valid[t & 1][0])[pw] = (uint16_t)bits16;
+                if (pw == 0) mbar_arrive_expect_tx(bar, KROUND);
                 else mbar_arrive(bar);
             }
-            if (lane < 4) {
-                const uint32_t dst = smem + RING0 + (uint32_t)slot * SLOT_BYTES + (uint32_t)(pw * 4 + lane) * 512u;
+            if (act) {
+                const uint32_t dst = smem + S_RING + (uint32_t)g * KROUND + (uint32_t)(pw * 4 + lane) * 512u;
 #pragma unroll
-                for (int cc = 0; cc < SLOT_CHUNKS; ++cc)
-                    tma_gather4(dst + (uint32_t)cc * KCHUNK_BYTES, tmap, (gi * SLOT_CHUNKS + cc) * 64, y[0], y[1], y[2],
-                                y[3], bar);
+                for (int cc = 0; cc < RCHUNKS; ++cc)
+                    tma_gather4(dst + (uint32_t)cc * KCHUNK, tmap, (g * RCHUNKS + cc) * 64, cur.y[0], cur.y[1], cur.y[2],
+                                cur.y[3], bar);
             }
         }
         if (!ok) break;
+        if (t + 1 < u.ntiles) {
+            cur = resolve_slots(p, raw);                        // loaded one tile ago
+            if (t + 2 < u.ntiles) raw = load_slots(p, u, tile_key0(u, t + 2) + koff, act);
+        }
     }
+    // Every round issued was consumed, unless a wait timed out: then give
+    // the gathers in flight time to land before the CTA can exit.
+    if (!ok) settle_copies();
 }
 
-// MMA issue (warp 16, lane 0): S[buf] = Q K^T per S tile, chunk by chunk:
-// 32 MMAs with Q's no-PE dims from TMEM, then 4 with Q's RoPE dims from
-// shared memory; each chunk's slot is released by a commit.
-__device__ void s_role_mma(const Params &p, Header *h, uint32_t smem, uint32_t tmem, const Unit &u)
+// ------------------------------------------------------------------ S role: MMA issue (warp 24, lane 0)
+//
+// S[buf] = Q K^T round by round: 32 MMAs with Q's no-PE dims from TMEM, then
+// 4 with Q's RoPE dims from shared memory; each round is released by a commit.
+__device__ void s_mma(const Params &p, Header *h, uint32_t smem, uint32_t tmem, const Unit &u)
 {
-    for (int t = 0; t < u.ntiles_s; ++t) {
+    for (int t = 0; t < u.ntiles; ++t) {
         const int buf = t & 1;
-        if (t >= 2 && !wait_bar(h, smem_u32(&h->s_free[buf]), (uint32_t)((t >> 1) - 1) & 1u, p.status, false)) break;
+        if (t >= 2 && !wait_bar(h, smem_u32(&h->s_free[buf]), (uint32_t)((t >> 1) - 1) & 1u, p.status)) break;
         const uint32_t d = tmem + TM_S0 + 128u * (uint32_t)buf;
         bool ok = true;
-        for (int c = 0; c < (int)K_CHUNKS; ++c) {
-            const int q = t * ((int)K_CHUNKS / SLOT_CHUNKS) + c / SLOT_CHUNKS, slot = q % NSLOT, use = q / NSLOT;
-            if (c % SLOT_CHUNKS == 0) {
-                if (!wait_bar(h, smem_u32(&h->c_full[slot]), (uint32_t)use & 1u, p.status, false)) { ok = false; break; }
-                tc_fence_after_sync();   // K arrives by TMA (async proxy): no proxy fence needed before the MMAs
-            }
-            if (c == 0) {
+#pragma unroll 1
+        for (int g = 0; g < NKR; ++g) {
+            if (!wait_bar(h, smem_u32(&h->c_full[g]), (uint32_t)t & 1u, p.status)) { ok = false; break; }
+            tc_fence_after_sync();
+            if (g == 0) {
                 volatile uint64_t *src = &h->t_valid[t & 1][0];
                 volatile uint64_t *dst = &h->s_valid[buf][0];
                 dst[0] = src[0];
                 dst[1] = src[1];
             }
-            const uint32_t sb = smem + RING0 + (uint32_t)slot * SLOT_BYTES + (uint32_t)(c % SLOT_CHUNKS) * KCHUNK_BYTES;
-            if (c < (int)V_CHUNKS) {
 #pragma unroll
-                for (int k = 0; k < 4; ++k)
-                    mma_ts(d, tmem + TM_Q + 32u * (uint32_t)c + 8u * (uint32_t)k, sdesc_sw128(sb + 32u * k, 16u, 1024u),
-                           IDESC_S, (c > 0 || k > 0) ? 1u : 0u);
-            } else {
+            for (int cc = 0; cc < RCHUNKS; ++cc) {
+                const int c = g * RCHUNKS + cc;
+                const uint32_t sb = smem + S_RING + (uint32_t)g * KROUND + (uint32_t)cc * KCHUNK;
+                if (c < 8) {
+                    const uint32_t a = tmem + 32u * (uint32_t)c;
 #pragma unroll
-                for (int k = 0; k < 4; ++k)
-                    mma_ss(d, sdesc_sw128(smem + QPE0 + 32u * k, 16u, 1024u), sdesc_sw128(sb + 32u * k, 16u, 1024u),
-                           IDESC_S, 1u);
+                    for (int k = 0; k < 4; ++k)
+                        mma_ts(d, a + 8u * (uint32_t)k, sdesc_sw128(sb + 32u * (uint32_t)k, 16u, 1024u), IDESC_S,
+                               (c | k) ? 1u : 0u);
+                } else {
+#pragma unroll
+                    for (int k = 0; k < 4; ++k)
+                        mma_ss(d, sdesc_sw128(smem + S_QPE + 32u * (uint32_t)k, 16u, 1024u),
+                               sdesc_sw128(sb + 32u * (uint32_t)k, 16u, 1024u), IDESC_S, 1u);
+                }
             }
-            if (c % SLOT_CHUNKS == SLOT_CHUNKS - 1) mma_commit(smem_u32(&h->c_empty[slot]));
+            mma_commit(smem_u32(&h->c_empty[g]));
         }
         if (!ok) break;
         mma_commit(smem_u32(&h->s_full[buf]));
@@ -380,30 +357,65 @@ __device__ void s_role_mma(const Params &p, Header *h, uint32_t smem, uint32_t t
     wait_bar(h, smem_u32(&h->drain), 0u, p.status, false, false);
 }
 
-// Softmax warps 0-7 (thread = row; warp group g = warp / 4 owns keys
-// [64g, 64g + 64) of every S tile and always fills the partner's P buffer g,
-// i.e. the partner consumes an S tile as two 64-key P halves).  Pass 1 reads
-// the whole score row (the other group's half first) for the maximum, which
-// both groups therefore agree on without exchanging data; pass 2 re-reads
-// the group's own 64 scores for the exponentials.  Q goes in first: the
-// no-PE dims to TMEM, the RoPE dims to shared memory.  After the last tile
-// the groups add their partial sums; group 0 writes the lse to the
-// workspace and 1/l to the partner.
-__device__ void s_role_rows(const Params &p, Header *h, uint32_t smem, uint32_t tmem, const Unit &u)
+// ------------------------------------------------------------------ S role: softmax (warps 0-7)
+
+// nbits (<= 64) mask bits starting at bit index bit0 as raw bytes (loads
+// only), and their combination into a word (bit n = bit bit0 + n).
+struct MaskBytes {
+    uint32_t b[9];
+    int sh, nbits;
+};
+
+__device__ __forceinline__ MaskBytes load_mask(const uint8_t *mask, int64_t bit0, int nbits)
+{
+    MaskBytes m;
+    m.sh = (int)(bit0 & 7);
+    m.nbits = nbits;
+    const int64_t first = bit0 >> 3;
+    const int nb = nbits > 0 ? (int)(((bit0 + nbits - 1) >> 3) - first + 1) : 0;
+#pragma unroll
+    for (int k = 0; k < 9; ++k) m.b[k] = k < nb ? (uint32_t)__ldg(mask + first + k) : 0u;
+    return m;
+}
+
+__device__ __forceinline__ uint64_t mask_word(const MaskBytes &m)
+{
+    uint64_t lo = 0;
+#pragma unroll
+    for (int k = 0; k < 8; ++k) lo |= (uint64_t)m.b[k] << (8 * k);
+    uint64_t w = m.sh ? ((lo >> m.sh) | ((uint64_t)m.b[8] << (64 - m.sh))) : lo;
+    if (m.nbits < 64) w &= m.nbits > 0 ? (1ull << m.nbits) - 1ull : 0ull;
+    return w;
+}
+
+// Thread = row r (TMEM lane), group g = warp / 4 owns keys [64g, 64g + 64)
+// of every S tile.  Per tile: read the group's 64 scores once into
+// registers (which frees the S buffer for the next MMAs), exchange the
+// row's partial maximum with the other group through shared memory, write
+// P = 2^(s*scale*log2e - m) as bf16 into the group's staging slot (K-major,
+// 128-byte swizzled: the A operand of the partner's P V MMAs), and the
+// group's leader ships it with one bulk copy.  Q goes in first: no-PE dims
+// to TMEM, RoPE dims to shared memory.
+__device__ void s_softmax(const Params &p, Header *h, uint32_t smem, uint32_t tmem, const Unit &u)
 {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int quad = warp & 3, grp = warp >> 2;
     const int r = quad * 32 + lane;
+    const bool leader = (threadIdx.x & 127) == 0;
     const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
     const int H = p.num_heads;
     const int64_t lr = u.r0 + r;
     const bool row_ok = lr < u.rows_b;
     const int64_t i = row_ok ? lr / H : 0;
     const int64_t hh = row_ok ? lr % H : 0;
+    // A negative scale is folded into Q (exact sign flips) so the score
+    // scale below is >= 0 and the maximum of s is the maximum of s * scale.
+    const uint32_t qsign = p.sm_scale < 0.f ? 0x80008000u : 0u;
+    const float sl2 = fabsf(p.sm_scale) * LOG2E;
 
-    // Q row: dims 0..511 -> TMEM columns [0, 256) (32-bit column k/2 holds
-    // elements k, k+1; group 0 writes dims 0..255, group 1 dims 256..511);
-    // dims 512..575 -> shared memory, K-major 128-byte swizzled (group 1).
+    // Q row: dims 0..511 -> TMEM columns [0, 256) (column k/2 holds elements
+    // k, k+1; group 0 writes dims 0..255, group 1 dims 256..511); dims
+    // 512..575 -> shared memory, K-major 128-byte swizzled (group 1).
     const __nv_bfloat16 *qrow = p.q + (u.qo0 + i) * p.q_stride_tok + hh * p.q_stride_head;
 #pragma unroll 1
     for (int c = grp * 4; c < grp * 4 + 4; ++c) {
@@ -412,16 +424,17 @@ __device__ void s_role_rows(const Params &p, Header *h, uint32_t smem, uint32_t 
         for (int v = 0; v < 8; ++v) {
             uint4 x = make_uint4(0u, 0u, 0u, 0u);
             if (row_ok) x = __ldg(reinterpret_cast<const uint4 *>(qrow + c * 64 + v * 8));
-            w[4 * v] = x.x; w[4 * v + 1] = x.y; w[4 * v + 2] = x.z; w[4 * v + 3] = x.w;
+            w[4 * v] = x.x ^ qsign; w[4 * v + 1] = x.y ^ qsign; w[4 * v + 2] = x.z ^ qsign; w[4 * v + 3] = x.w ^ qsign;
         }
-        tmem_st32(tmem + lane_base + TM_Q + 32u * (uint32_t)c, w);
+        tmem_st32(tmem + lane_base + 32u * (uint32_t)c, w);
     }
     if (grp == 1) {
-        uint8_t *qpe = reinterpret_cast<uint8_t *>(h) + QPE0 + (r >> 3) * 1024 + (r & 7) * 128;
+        uint8_t *qpe = reinterpret_cast<uint8_t *>(h) + S_QPE + (r >> 3) * 1024 + (r & 7) * 128;
 #pragma unroll
         for (int v = 0; v < 8; ++v) {
             uint4 x = make_uint4(0u, 0u, 0u, 0u);
             if (row_ok) x = __ldg(reinterpret_cast<const uint4 *>(qrow + 512 + v * 8));
+            x.x ^= qsign; x.y ^= qsign; x.z ^= qsign; x.w ^= qsign;
             *reinterpret_cast<uint4 *>(qpe + ((v ^ (r & 7)) << 4)) = x;
         }
         fence_proxy_async_smem();
@@ -431,114 +444,122 @@ __device__ void s_role_rows(const Params &p, Header *h, uint32_t smem, uint32_t 
     named_barrier_sync(1, SOFTMAX_THREADS + 32);
 
     const int64_t mrow = p.mask_indptr[u.b] + i * u.N;
-    const float sl2 = p.sm_scale * LOG2E;
-    const uint32_t peer_pbuf = map_cluster(smem + PBUF0, 1) + (uint32_t)grp * P_BUF;
-    const uint32_t peer_alpha = map_cluster(smem_u32(&h->alpha[grp][0]), 1);
-    const uint32_t peer_flags = map_cluster(smem_u32(&h->flags[grp]), 1);
+    uint8_t *stage = reinterpret_cast<uint8_t *>(h) + S_STAGE + (uint32_t)grp * PSLOT;
+    uint8_t *prow = stage + (r >> 3) * 1024 + (r & 7) * 128;
+    const uint32_t stage_u32 = smem + S_STAGE + (uint32_t)grp * PSLOT;
+    const uint32_t copy_bytes = grp == 0 ? PTILE + SIDE_BYTES : PTILE;
+    float *xmax = reinterpret_cast<float *>(reinterpret_cast<uint8_t *>(h) + S_XMAX);
     float m_used = -INFINITY, l = 0.f;
     bool ok = true;
-    // Mask bits of S tile t for this row (two 64-bit words), loaded one tile ahead.
-    struct Bits { uint64_t w[2]; };
-    auto mask_of = [&](int t) -> Bits {
-        Bits b{{0ull, 0ull}};
-        if (row_ok && t < u.ntiles_s) {
-#pragma unroll
-            for (int hf = 0; hf < 2; ++hf) {
-                const int64_t j0 = tile_key0(u, t) + 64 * hf;
-                const int64_t nk = u.k1 - j0;
-                b.w[hf] = load_bits(p.custom_mask, mrow + j0, (int)(nk < 64 ? (nk > 0 ? nk : 0) : 64));
-            }
-        }
-        return b;
-    };
-    Bits next_bits = mask_of(0);
 
-    for (int t = 0; t < u.ntiles_s; ++t) {
+    // This group's mask bits of a tile: bytes loaded a tile ahead, combined after use.
+    auto mask_of = [&](int t) -> MaskBytes {
+        const int64_t j0 = tile_key0(u, t) + 64 * grp;
+        const int64_t nk = u.k1 - j0;
+        return load_mask(p.custom_mask, mrow + j0, row_ok ? (int)(nk < 64 ? (nk > 0 ? nk : 0) : 64) : 0);
+    };
+    uint64_t bits = mask_word(mask_of(0));
+    MaskBytes nm = mask_of(u.ntiles > 1 ? 1 : 0);
+
+    for (int t = 0; t < u.ntiles; ++t) {
         const int buf = t & 1;
-        const Bits bits = next_bits;
-        next_bits = mask_of(t + 1);
-        if (!warp_wait(h, smem_u32(&h->s_full[buf]), (uint32_t)(t >> 1) & 1u, p.status, false)) { ok = false; break; }
+        const bool got = warp_wait(h, smem_u32(&h->s_full[buf]), (uint32_t)(t >> 1) & 1u, p.status);
         tc_fence_after_sync();
-        const uint32_t s_col = tmem + lane_base + TM_S0 + 128u * (uint32_t)buf;
-        uint64_t vis[2];
-        vis[0] = *reinterpret_cast<volatile uint64_t *>(&h->s_valid[buf][0]) & bits.w[0];
-        vis[1] = *reinterpret_cast<volatile uint64_t *>(&h->s_valid[buf][1]) & bits.w[1];
-        const bool all_vis = __all_sync(0xffffffffu, (vis[0] & vis[1]) == ~0ull);
-        uint32_t sv[32];
-        // pass 1: maximum over all 128 scores, the other group's half first
-        float mx = -INFINITY;
+        const uint32_t s_col = tmem + lane_base + TM_S0 + 128u * (uint32_t)buf + 64u * (uint32_t)grp;
+        uint32_t sa[32], sb[32];
+        tmem_ld32(s_col, sa);
+        tmem_ld32(s_col + 32u, sb);
+        const uint64_t vis = *reinterpret_cast<volatile uint64_t *>(&h->s_valid[buf][grp]) & bits;
+        tmem_ld_wait();
+        // The scores are in registers: the MMAs may refill this S buffer.
+        tc_fence_before_sync();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&h->s_free[buf]));
+        const bool all_vis = __all_sync(0xffffffffu, vis == ~0ull);
+        const uint32_t v0 = (uint32_t)vis, v1 = (uint32_t)(vis >> 32);
+
+        float lmax = -INFINITY;
+        if (all_vis) {
 #pragma unroll
-        for (int part = 0; part < 4; ++part) {
-            const int half = (part < 2) ? 1 - grp : grp;
-            const int q = 2 * half + (part & 1);        // 32-column quarter of the row
-            tmem_ld32(s_col + 32u * (uint32_t)q, sv);
-            tmem_ld_wait();
-            const uint32_t vq = (uint32_t)(vis[half] >> (32 * (q & 1)));
-            if (all_vis) {
+            for (int n = 0; n < 32; ++n) lmax = fmaxf(lmax, fmaxf(__uint_as_float(sa[n]), __uint_as_float(sb[n])));
+        } else {
 #pragma unroll
-                for (int n = 0; n < 32; ++n) mx = fmaxf(mx, __uint_as_float(sv[n]));
-            } else {
-#pragma unroll
-                for (int n = 0; n < 32; ++n) mx = fmaxf(mx, ((vq >> n) & 1u) ? __uint_as_float(sv[n]) : -INFINITY);
+            for (int n = 0; n < 32; ++n) {
+                lmax = fmaxf(lmax, ((v0 >> n) & 1u) ? __uint_as_float(sa[n]) : -INFINITY);
+                lmax = fmaxf(lmax, ((v1 >> n) & 1u) ? __uint_as_float(sb[n]) : -INFINITY);
             }
         }
-        mx *= sl2;                                 // maximum in log2 units (sl2 > 0 keeps the order)
+        xmax[(buf * 2 + grp) * ROWS + r] = lmax;
+        // The staging slot is free once the previous bulk copy has read it.
+        if (leader) bulk_wait_read_all();
+        // Both groups: maxima exchanged, staging slots free; all agree to go on.
+        if (!named_barrier_and(5, SOFTMAX_THREADS, got)) { ok = false; break; }
+        float mx = fmaxf(lmax, xmax[(buf * 2 + (1 - grp)) * ROWS + r]);
+        mx = mx == -INFINITY ? -INFINITY : mx * sl2;   // log2 units
         float alpha = 1.f;
         bool rescale = false;
-        if (mx > m_used + RESCALE_LOG2) {        // also the first tile where the row sees a key
+        if (mx > m_used + RESCALE_LOG2) {              // also the first tile where the row sees a key
             alpha = (m_used == -INFINITY) ? 0.f : ex2_approx(m_used - mx);
             l *= alpha;
             m_used = mx;
             rescale = true;
         }
-        // The partner must be done with P buffer grp (this group's half of the previous S tile).
-        if (t >= 1 && !warp_wait(h, smem_u32(&h->p_empty[grp]), (uint32_t)(t - 1) & 1u, p.status, true)) {
-            ok = false;
-            break;
-        }
-        // pass 2: p = 2^(s * sl2 - m_used) for this group's 64 keys; masked scores give 0.
+
+        // p = 2^(s * sl2 - m_used) for this group's 64 keys; masked keys give 0.
         const float neg_m = m_used == -INFINITY ? 0.f : -m_used;
-        const uint32_t prow = peer_pbuf + (uint32_t)(r >> 3) * 1024u + (uint32_t)(r & 7) * 128u;
         float psum = 0.f;
 #pragma unroll
         for (int part = 0; part < 2; ++part) {
-            tmem_ld32(s_col + 32u * (uint32_t)(2 * grp + part), sv);
-            tmem_ld_wait();
-            const uint32_t vq = (uint32_t)(vis[grp] >> (32 * part));
+            const uint32_t *sv = part ? sb : sa;
+            const uint32_t vq = part ? v1 : v0;
             uint32_t pk[16];
 #pragma unroll
             for (int n = 0; n < 16; ++n) {
-                const float a0 = (all_vis || ((vq >> (2 * n)) & 1u)) ? __uint_as_float(sv[2 * n]) : -INFINITY;
-                const float a1 = (all_vis || ((vq >> (2 * n + 1)) & 1u)) ? __uint_as_float(sv[2 * n + 1]) : -INFINITY;
-                const float p0 = ex2_approx(fmaf(a0, sl2, neg_m));
-                const float p1 = ex2_approx(fmaf(a1, sl2, neg_m));
+                float p0 = ex2_approx(fmaf(__uint_as_float(sv[2 * n]), sl2, neg_m));
+                float p1 = ex2_approx(fmaf(__uint_as_float(sv[2 * n + 1]), sl2, neg_m));
+                if (!all_vis) {
+                    p0 = ((vq >> (2 * n)) & 1u) ? p0 : 0.f;
+                    p1 = ((vq >> (2 * n + 1)) & 1u) ? p1 : 0.f;
+                }
                 psum += p0 + p1;
                 pk[n] = pack_bf16x2(p0, p1);
             }
-            // keys 32*part .. 32*part+31 of this group's half: 16-B pieces 4*part .. 4*part+3 of row r
+            // keys 32*part .. +31 of this half: 16-B pieces 4*part .. 4*part+3 of row r
 #pragma unroll
             for (int qq = 0; qq < 4; ++qq)
-                st_cluster_v4(prow + ((((uint32_t)(4 * part + qq)) ^ (uint32_t)(r & 7)) << 4), pk[4 * qq],
-                              pk[4 * qq + 1], pk[4 * qq + 2], pk[4 * qq + 3]);
+                *reinterpret_cast<uint4 *>(prow + ((((uint32_t)(4 * part + qq)) ^ (uint32_t)(r & 7)) << 4)) =
+                    make_uint4(pk[4 * qq], pk[4 * qq + 1], pk[4 * qq + 2], pk[4 * qq + 3]);
         }
-        tc_fence_before_sync();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(smem_u32(&h->s_free[buf]));
         l += psum;
-        // The O tile of group 0's half rescales O first; group 1's half follows with the same maximum.
-        st_cluster_f32(peer_alpha + (uint32_t)r * 4u, (grp == 0 && rescale) ? alpha : 1.f);
-        const uint32_t any = (grp == 0 && __any_sync(0xffffffffu, rescale)) ? 1u : 0u;
-        if (lane == 0) st_cluster_u8(peer_flags + (uint32_t)quad, any);
-        __syncwarp();
-        if (lane == 0) mbar_arrive(smem_u32(&h->p_written[grp]));
+        if (grp == 0) {
+            // The first half's O tile rescales O; the second half follows with the same maximum.
+            reinterpret_cast<float *>(stage + PTILE)[r] = rescale ? alpha : 1.f;
+            const uint32_t any = __any_sync(0xffffffffu, rescale) ? 1u : 0u;
+            if (lane == 0) reinterpret_cast<uint32_t *>(stage + PTILE + ROWS * 4)[quad] = any;
+        }
+        fence_proxy_async_smem();
+        // The partner must be done with P slot [grp][t & 1] (its use two tiles ago).
+        bool slot_free = true;
+        if (leader && t >= 2)
+            slot_free = wait_bar(h, smem_u32(&h->p_empty[grp][buf]), (uint32_t)((t >> 1) - 1) & 1u, p.status);
+        // Both groups vote here too, so they always leave the loop together.
+        if (!named_barrier_and(6, SOFTMAX_THREADS, slot_free)) { ok = false; break; }
+        if (leader) {
+            bulk_copy_to_cluster(map_cluster(smem + O_PSLOT + (uint32_t)(2 * grp + buf) * PSLOT, 1), stage_u32,
+                                 copy_bytes, map_cluster(smem_u32(&h->p_full[grp][buf]), 1));
+            bulk_commit_group();
+        }
+        // mask bits of tile t + 1 (loaded during this tile), then the loads for t + 2
+        bits = mask_word(nm);
+        if (t + 2 < u.ntiles) nm = mask_of(t + 2);
     }
+    if (leader) bulk_wait_read_all();
 
     // Partial sums of group 1 -> group 0 (both groups always reach this barrier).
-    float *lpart = reinterpret_cast<float *>(reinterpret_cast<uint8_t *>(h) + S_SCRATCH);
-    if (grp == 1) lpart[r] = l;
-    named_barrier_sync(2, SOFTMAX_THREADS);
+    if (grp == 1) h->lpart[r] = l;
+    named_barrier_sync(4, SOFTMAX_THREADS);
     if (grp == 1) return;
-    l += lpart[r];
+    l += h->lpart[r];
     if (ok && row_ok) {
         const int64_t row = u.qo0 * H + lr;
         if (row < p.rows_cap)
@@ -549,90 +570,131 @@ __device__ void s_role_rows(const Params &p, Header *h, uint32_t smem, uint32_t 
     if (lane == 0) mbar_arrive_cluster(smem_u32(&h->l_ready), 1);
 }
 
-// Sender (warp 17, lane 0): once a softmax group stored its P half into the
-// partner, order those writes for the partner's tensor-core reads and
-// publish the O tile.  Keeps the proxy fence and the cluster-scope release
-// off the softmax warps.
-__device__ void s_role_sender(const Params &p, Header *h, const Unit &u)
+// ------------------------------------------------------------------ O role: gather (warps 8-23)
+//
+// V half tile layout: four 64-dim column blocks of 64 keys (8 KB each, key
+// rows of 128 B swizzled as above): the MN-major B operand of one N = 256
+// P V MMA.  Round R = 2 * (O tile) + half goes to ring slot R % 4; team k
+// issues the rounds of half k.  Team warp w, lane l (0-3) gathers key group
+// (4w + l) / 2 (four keys) for column blocks 2 (l & 1) and 2 (l & 1) + 1.
+__device__ void o_gather(const Params &p, Header *h, const CUtensorMap *tmap, uint32_t smem, const Unit &u)
 {
-    for (int t = 0; t < u.ntiles; ++t) {
-        const int buf = t & 1;
-        if (!wait_bar(h, smem_u32(&h->p_written[buf]), (uint32_t)(t >> 1) & 1u, p.status, false)) break;
-        fence_proxy_async_cluster();
-        mbar_arrive_cluster(smem_u32(&h->p_full[buf]), 1);
+    const int pwa = (int)(threadIdx.x >> 5) - PRODUCER_WARP0;
+    const int team = pwa / TEAM_WARPS, pw = pwa % TEAM_WARPS;
+    const int lane = threadIdx.x & 31;
+    const bool act = lane < 4;
+    const int kg = (pw * 4 + lane) >> 1, blk0 = (lane & 1) * 2;
+    const int nt = 2 * u.ntiles;
+    auto key0 = [&](int ot) { return tile_key0(u, ot >> 1) + (int64_t)(ot & 1) * KEYS_O + kg * 4; };
+    RawSlots raw = load_slots(p, u, key0(0), act);
+    Slots cur = resolve_slots(p, raw);
+    raw = load_slots(p, u, key0(1), act);
+    bool ok = true;
+    for (int ot = 0; ot < nt; ++ot) {
+        const int R = 2 * ot + team, slot = R % NVH, use = R / NVH;
+        if (use > 0 && !__all_sync(0xffffffffu, wait_bar(h, smem_u32(&h->v_empty[slot]), (uint32_t)(use - 1) & 1u, p.status))) {
+            ok = false;
+            break;
+        }
+        const uint32_t bar = smem_u32(&h->v_full[slot]);
+        if (lane == 0) {
+            if (pw == 0) mbar_arrive_expect_tx(bar, VHALF);
+            else mbar_arrive(bar);
+        }
+        if (act) {
+            const uint32_t dst = smem + O_VRING + (uint32_t)slot * VHALF + (uint32_t)kg * 512u;
+#pragma unroll
+            for (int j = 0; j < 2; ++j)
+                tma_gather4(dst + (uint32_t)(blk0 + j) * VCHUNK, tmap, (4 * team + blk0 + j) * 64, cur.y[0], cur.y[1],
+                            cur.y[2], cur.y[3], bar);
+        }
+        if (ot + 1 < nt) {
+            cur = resolve_slots(p, raw);
+            if (ot + 2 < nt) raw = load_slots(p, u, key0(ot + 2), act);
+        }
     }
+    if (!ok) settle_copies();
 }
 
-// ------------------------------------------------------------------ O role
-
-// MMA issue (warp 16, lane 0): O += P V for every tile, both 256-column halves.
-__device__ void o_role_mma(const Params &p, Header *h, uint32_t smem, uint32_t tmem, const Unit &u)
+// ------------------------------------------------------------------ O role: MMA issue (warp 16, lane 0)
+//
+// O += P V per 64-key O tile: two halves of the value dims, N = 256 each.
+// P slot [g][par] of O tile ot: g = ot & 1 (softmax group), par = (ot >> 1) & 1.
+__device__ void o_mma(const Params &p, Header *h, uint32_t smem, uint32_t tmem, const Unit &u)
 {
-    uint32_t nrs = 0;
-    for (int t = 0; t < u.ntiles; ++t) {
-        const int stage = t % STAGES, buf = t & 1;
-        if (!wait_bar(h, smem_u32(&h->v_full[stage]), (uint32_t)(t / STAGES) & 1u, p.status, false)) break;
-        if (!wait_bar(h, smem_u32(&h->p_full[buf]), (uint32_t)(t >> 1) & 1u, p.status, true)) break;
-        const uint32_t flags = t > 0 ? *reinterpret_cast<volatile uint32_t *>(&h->flags[buf]) : 0u;
-        if (flags) {
-            mma_commit(smem_u32(&h->pv_sync));
-            if (!wait_bar(h, smem_u32(&h->pv_sync), nrs & 1u, p.status, false)) break;
-            mbar_arrive(smem_u32(&h->rs_req));
-            if (!wait_bar(h, smem_u32(&h->rs_done), nrs & 1u, p.status, false)) break;
-            ++nrs;
-        }
-        tc_fence_after_sync();
-        fence_proxy_async_smem();
-        const uint32_t pb = smem + PBUF0 + (uint32_t)buf * P_BUF;
-        const uint32_t vb = smem + STAGE0 + (uint32_t)stage * V_STAGE;
-#pragma unroll
-        for (int k = 0; k < KEYS / 16; ++k) {
-            const uint64_t adesc = sdesc_sw128(pb + 32u * (uint32_t)k, 16u, 1024u);
-#pragma unroll
-            for (int half = 0; half < 2; ++half) {
-                const uint64_t bdesc =
-                    sdesc_sw128(vb + (uint32_t)half * 4u * CHUNK_BYTES + (uint32_t)k * 16u * 128u, CHUNK_BYTES, 1024u);
-                mma_ss(tmem + 256u * (uint32_t)half, adesc, bdesc, IDESC_PV, (t > 0 || k > 0) ? 1u : 0u);
+    const int nt = 2 * u.ntiles;
+    int slot = 0;
+    uint32_t phase = 0, nrs = 0;
+    uint32_t pphase = 0;       // bit 2g + par: parity of P slot [g][par]'s pending transfer
+    bool ok = true;
+    for (int ot = 0; ot < nt && ok; ++ot) {
+        const int g = ot & 1, par = (ot >> 1) & 1;
+        if (!wait_bar(h, smem_u32(&h->p_full[g][par]), (pphase >> (2 * g + par)) & 1u, p.status)) { ok = false; break; }
+        pphase ^= 1u << (2 * g + par);
+        const uint32_t pb = smem + O_PSLOT + (uint32_t)(2 * g + par) * PSLOT;
+        if (g == 0 && ot > 0) {
+            const volatile uint32_t *f = reinterpret_cast<const volatile uint32_t *>(
+                reinterpret_cast<uint8_t *>(h) + O_PSLOT + (2 * g + par) * PSLOT + PTILE + ROWS * 4);
+            if (f[0] | f[1] | f[2] | f[3]) {
+                mma_commit(smem_u32(&h->pv_sync));
+                if (!wait_bar(h, smem_u32(&h->pv_sync), nrs & 1u, p.status)) { ok = false; break; }
+                *reinterpret_cast<volatile int32_t *>(&h->rs_slot) = par;
+                mbar_arrive(smem_u32(&h->rs_req));
+                if (!wait_bar(h, smem_u32(&h->rs_done), nrs & 1u, p.status)) { ok = false; break; }
+                ++nrs;
             }
         }
-        mma_commit(smem_u32(&h->v_empty[stage]));
-        mma_commit_multicast(smem_u32(&h->p_empty[buf]), (uint16_t)0x1);
+        tc_fence_after_sync();
+#pragma unroll 1
+        for (int hf = 0; hf < 2; ++hf) {
+            if (!wait_bar(h, smem_u32(&h->v_full[slot]), phase, p.status)) { ok = false; break; }
+            tc_fence_after_sync();
+            const uint32_t vb = smem + O_VRING + (uint32_t)slot * VHALF;
+#pragma unroll
+            for (int k = 0; k < KEYS_O / 16; ++k)
+                mma_ss(tmem + 256u * (uint32_t)hf, sdesc_sw128(pb + 32u * (uint32_t)k, 16u, 1024u),
+                       sdesc_sw128(vb + (uint32_t)k * 16u * 128u, VCHUNK, 1024u), IDESC_PV, (ot | k) ? 1u : 0u);
+            mma_commit(smem_u32(&h->v_empty[slot]));
+            if (++slot == NVH) { slot = 0; phase ^= 1u; }
+        }
+        if (!ok) break;
+        mma_commit_multicast(smem_u32(&h->p_empty[g][par]), (uint16_t)0x1);
+        // arm this slot for its next P transfer
+        mbar_arrive_expect_tx(smem_u32(&h->p_full[g][par]), g == 0 ? PTILE + SIDE_BYTES : PTILE);
     }
     mma_commit(smem_u32(&h->drain));
+    *reinterpret_cast<volatile int32_t *>(&h->rs_slot) = -1;
+    mbar_arrive(smem_u32(&h->rs_req));
+    if (!ok) settle_copies();   // P transfers already on their way land before the CTA can exit
 }
 
-// Row warps (thread = TMEM lane = row): rescale O rows on flagged tiles;
+// Row warps 0-3 (thread = TMEM lane = row): rescale O rows when asked;
 // after the last tile, O / l -> fp32 partial in the workspace.
-__device__ void o_role_rows(const Params &p, Header *h, uint32_t smem, uint32_t tmem, const Unit &u)
+__device__ void o_rows(const Params &p, Header *h, uint32_t smem, uint32_t tmem, const Unit &u)
 {
     const int r = threadIdx.x, warp = r >> 5, lane = r & 31;
     const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
-    uint32_t nrs = 0;
     bool ok = true;
-    for (int t = 0; t < u.ntiles; ++t) {
-        const int buf = t & 1;
-        if (!warp_wait(h, smem_u32(&h->p_full[buf]), (uint32_t)(t >> 1) & 1u, p.status, true)) { ok = false; break; }
-        const uint32_t flags = t > 0 ? *reinterpret_cast<volatile uint32_t *>(&h->flags[buf]) : 0u;
-        if (flags) {
-            const float a = h->alpha[buf][r];
-            if (!warp_wait(h, smem_u32(&h->rs_req), nrs & 1u, p.status, false)) { ok = false; break; }
-            tc_fence_after_sync();
+    for (uint32_t n = 0;; ++n) {
+        if (!warp_wait(h, smem_u32(&h->rs_req), n & 1u, p.status)) { ok = false; break; }
+        const int par = *reinterpret_cast<volatile int32_t *>(&h->rs_slot);
+        if (par < 0) break;
+        const float a = reinterpret_cast<const float *>(reinterpret_cast<uint8_t *>(h) + O_PSLOT +
+                                                        (uint32_t)par * PSLOT + PTILE)[r];
+        tc_fence_after_sync();
 #pragma unroll 1
-            for (int c = 0; c < DV / 32; ++c) {
-                uint32_t v[32];
-                tmem_ld32(tmem + lane_base + 32u * (uint32_t)c, v);
-                tmem_ld_wait();
+        for (int c = 0; c < DV / 32; ++c) {
+            uint32_t v[32];
+            tmem_ld32(tmem + lane_base + 32u * (uint32_t)c, v);
+            tmem_ld_wait();
 #pragma unroll
-                for (int e = 0; e < 32; ++e) v[e] = __float_as_uint(__uint_as_float(v[e]) * a);
-                tmem_st32(tmem + lane_base + 32u * (uint32_t)c, v);
-            }
-            tmem_st_wait();
-            tc_fence_before_sync();
-            mbar_arrive(smem_u32(&h->rs_done));
-            ++nrs;
+            for (int e = 0; e < 32; ++e) v[e] = __float_as_uint(__uint_as_float(v[e]) * a);
+            tmem_st32(tmem + lane_base + 32u * (uint32_t)c, v);
         }
+        tmem_st_wait();
+        tc_fence_before_sync();
         __syncwarp();
-        if (lane == 0) mbar_arrive_cluster(smem_u32(&h->p_empty[buf]), 0);
+        if (lane == 0) mbar_arrive(smem_u32(&h->rs_done));
     }
     if (!__all_sync(0xffffffffu, wait_bar(h, smem_u32(&h->drain), 0u, p.status, false, false))) ok = false;
     if (!warp_wait(h, smem_u32(&h->l_ready), 0u, p.status, true)) ok = false;
@@ -649,14 +711,10 @@ __device__ void o_role_rows(const Params &p, Header *h, uint32_t smem, uint32_t 
         tmem_ld_wait();
         if (write) {
 #pragma unroll
-            for (int e = 0; e < 8; ++e) {
-                float4 o;
-                o.x = __uint_as_float(v[4 * e]) * il;
-                o.y = __uint_as_float(v[4 * e + 1]) * il;
-                o.z = __uint_as_float(v[4 * e + 2]) * il;
-                o.w = __uint_as_float(v[4 * e + 3]) * il;
-                *reinterpret_cast<float4 *>(dst + c * 32 + 4 * e) = o;
-            }
+            for (int e = 0; e < 8; ++e)
+                *reinterpret_cast<float4 *>(dst + c * 32 + 4 * e) =
+                    make_float4(__uint_as_float(v[4 * e]) * il, __uint_as_float(v[4 * e + 1]) * il,
+                                __uint_as_float(v[4 * e + 2]) * il, __uint_as_float(v[4 * e + 3]) * il);
         }
     }
 }
@@ -671,11 +729,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
     const uint32_t role = cluster_rank();
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
-    // a1: segment decode.  Both CTAs of the pair compute the same unit, so
-    // they leave together when it is empty.
-    // Grid: x = 2 * row tile + rank in the pair, y = split, z = request.  Row
-    // tiles vary fastest, so pairs that read the same key chunk run together
-    // and share it through L2.
+    // Segment decode.  Both CTAs of the pair compute the same unit, so they
+    // leave together when it is empty.  Grid: x = 2 * row tile + rank in
+    // the pair, y = split, z = request; row tiles vary fastest, so pairs
+    // that read the same key chunk run together and share it through L2.
     Unit u;
     u.split = (int)blockIdx.y;
     u.b = (int)blockIdx.z;
@@ -695,37 +752,41 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
     u.k0 = (int64_t)u.split * chunk;
     if (u.k0 >= u.N) return;
     u.k1 = (u.k0 + chunk < u.N) ? u.k0 + chunk : u.N;
-    u.ntiles_s = (int)((u.k1 - u.k0 + KEYS_S - 1) / KEYS_S);
-    u.ntiles = 2 * u.ntiles_s;
+    u.ntiles = (int)((u.k1 - u.k0 + KEYS_S - 1) / KEYS_S);
     {
         const int64_t row_tiles = (u.rows_b + ROWS - 1) / ROWS;
-        u.rot = (int)(((int64_t)(blockIdx.x >> 1) * u.ntiles_s) / row_tiles);
+        u.rot = (int)(((int64_t)(blockIdx.x >> 1) * u.ntiles) / row_tiles);
     }
 
     if (tid == 0) {
-        for (int s = 0; s < NSLOT; ++s) {
-            mbar_init(smem_u32(&h->c_full[s]), PRODUCER_WARPS);
+        for (int s = 0; s < NKR; ++s) {
+            mbar_init(smem_u32(&h->c_full[s]), TEAM_WARPS);
             mbar_init(smem_u32(&h->c_empty[s]), 1);
         }
-        for (int s = 0; s < STAGES; ++s) {
-            mbar_init(smem_u32(&h->v_full[s]), PRODUCER_WARPS);
+        for (int s = 0; s < NVH; ++s) {
+            mbar_init(smem_u32(&h->v_full[s]), TEAM_WARPS);
             mbar_init(smem_u32(&h->v_empty[s]), 1);
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(smem_u32(&h->s_full[i]), 2);
             mbar_init(smem_u32(&h->s_free[i]), SOFTMAX_THREADS / 32);
-            mbar_init(smem_u32(&h->p_written[i]), SOFTMAX_THREADS / 64);
-            mbar_init(smem_u32(&h->p_empty[i]), 1 + 4);
-            mbar_init(smem_u32(&h->p_full[i]), 1);
-            h->flags[i] = 0u;
+            for (int j = 0; j < 2; ++j) {
+                mbar_init(smem_u32(&h->p_empty[i][j]), 1);
+                mbar_init(smem_u32(&h->p_full[i][j]), 1);
+            }
         }
         mbar_init(smem_u32(&h->pv_sync), 1);
         mbar_init(smem_u32(&h->rs_req), 1);
-        mbar_init(smem_u32(&h->rs_done), ROWS);
+        mbar_init(smem_u32(&h->rs_done), 4);
         mbar_init(smem_u32(&h->l_ready), 4);
         mbar_init(smem_u32(&h->drain), 1);
         h->abort = 0u;
+        h->rs_slot = 0;
         fence_mbar_init_cluster();
+        if (role == 1)   // the P slots expect their first transfers
+            for (int i = 0; i < 2; ++i)
+                for (int j = 0; j < 2; ++j)
+                    mbar_arrive_expect_tx(smem_u32(&h->p_full[i][j]), i == 0 ? PTILE + SIDE_BYTES : PTILE);
     }
     if (warp == PRODUCER_WARP0 && lane == 0) prefetch_tensormap(&pool_map);
     if (warp == MMA_WARP) {
@@ -738,26 +799,31 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
     tc_fence_after_sync();
     const uint32_t tmem = *reinterpret_cast<volatile uint32_t *>(&h->tmem_base);
 
-    if (role == 0) {
-        if (warp < PRODUCER_WARP0) {
-            s_role_rows(p, h, smem, tmem, u);
-        } else if (warp < MMA_WARP) {
-            s_role_gather(p, h, &pool_map, smem, u);
-        } else if (warp == MMA_WARP) {
-            named_barrier_sync(1, SOFTMAX_THREADS + 32);
-            tc_fence_after_sync();
-            if (lane == 0) s_role_mma(p, h, smem, tmem, u);
-        } else if (lane == 0) {
-            s_role_sender(p, h, u);
-        }
+    // Roles by warpgroup; setmaxnreg moves registers from the producer, MMA
+    // and idle warpgroups to the softmax / row warpgroups.
+    // Every warpgroup returns to the launch budget before the common exit.
+    const bool wide = role == 0 ? warp < PRODUCER_WARP0 : warp < 4;
+    if (wide) {
+        regs_inc<REGS_WIDE>();
+        if (role == 0) s_softmax(p, h, smem, tmem, u);
+        else o_rows(p, h, smem, tmem, u);
+        regs_dec<LAUNCH_REGS>();
     } else {
-        if (warp < 4) {
-            o_role_rows(p, h, smem, tmem, u);
-        } else if (warp >= PRODUCER_WARP0 && warp < MMA_WARP) {
-            gather_tiles<V_CHUNKS>(p, h, &pool_map, smem + STAGE0, V_STAGE, h->v_full, h->v_empty, nullptr, u);
-        } else if (warp == MMA_WARP && lane == 0) {
-            o_role_mma(p, h, smem, tmem, u);
+        regs_dec<REGS_NARROW>();
+        if (warp >= PRODUCER_WARP0 && warp < MMA_WARP) {
+            if (role == 0) s_gather(p, h, &pool_map, smem, u);
+            else o_gather(p, h, &pool_map, smem, u);
+        } else if (warp == MMA_WARP) {
+            if (role == 0) {
+                named_barrier_sync(1, SOFTMAX_THREADS + 32);
+                tc_fence_after_sync();
+                if (lane == 0) s_mma(p, h, smem, tmem, u);
+            } else if (lane == 0) {
+                o_mma(p, h, smem, tmem, u);
+            }
         }
+        __syncwarp();
+        regs_inc<LAUNCH_REGS>();
     }
 
     tc_fence_before_sync();
@@ -769,7 +835,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
         tmem_dealloc(tmem, TMEM_COLS);
     }
 }
-
 
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 std::once_flag g_encode_once;
@@ -801,6 +866,12 @@ cudaError_t tc_init()
             g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
     });
     if (g_encode == nullptr) return cudaErrorNotSupported;
+    // setmaxnreg.inc waits for registers the CTA does not have if the
+    // launch allocation is smaller than the split assumes: refuse to run.
+    cudaFuncAttributes fa;
+    cudaError_t e = cudaFuncGetAttributes(&fa, tc_split_kernel);
+    if (e != cudaSuccess) return e;
+    if (fa.numRegs < LAUNCH_REGS || fa.maxThreadsPerBlock < THREADS) return cudaErrorNotSupported;
     return cudaFuncSetAttribute(tc_split_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_ALLOC);
 }
 
