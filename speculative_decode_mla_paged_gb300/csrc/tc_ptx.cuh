@@ -202,6 +202,19 @@ __device__ __forceinline__ void tma_gather4(uint32_t dst, const void *tmap, int 
         : "memory");
 }
 
+// The same gather delivered to the same shared-memory offset, and counted on
+// the barrier at the same offset, in every CTA of `cta_mask` in the cluster.
+__device__ __forceinline__ void tma_gather4_multicast(uint32_t dst, const void *tmap, int x, int y0, int y1, int y2,
+                                                      int y3, uint32_t bar, uint16_t cta_mask)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes.multicast::cluster "
+        "[%0], [%1, {%2, %3, %4, %5, %6}], [%7], %8;"
+        ::"r"(dst), "l"(reinterpret_cast<uint64_t>(tmap)), "r"(x), "r"(y0), "r"(y1), "r"(y2), "r"(y3), "r"(bar),
+          "h"(cta_mask)
+        : "memory");
+}
+
 __device__ __forceinline__ void prefetch_tensormap(const void *tmap)
 {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(tmap)) : "memory");

@@ -1,17 +1,19 @@
 // Tensor-core split kernel for tree-verify attention (sm_103a: tcgen05, TMEM,
 // TMA gathers, bulk copies between the CTAs of a cluster).
 //
-// Work unit: one (key split, 128-row tile, request), the same unit as the
-// pages' split-KV flash-decode partial ("The Capture-Safe Kernel",
-// Decision 3), but every key tile is loaded once per 128 rows (T*H rows of
-// one request share all keys: MLA latent attention, "The Integration
-// Chasm", section Decision) and both contractions run on the tensor cores.
+// Work unit: one (key split, pair of 128-row tiles, request), the same
+// unit as the pages' split-KV flash-decode partial ("The Capture-Safe
+// Kernel", Decision 3), but every key tile is loaded once per 256 rows (T*H
+// rows of one request share all keys: MLA latent attention, "The
+// Integration Chasm", section Decision) and both contractions run on the
+// tensor cores.
 //
-// Why a 2-CTA cluster per unit.  A 128 x 512 fp32 output accumulator is the
-// whole of an SM's TMEM (128 lanes x 512 columns), so one SM cannot hold Q,
-// the scores S and O for 128 rows.  The pair splits the work by role:
+// A 4-CTA cluster per unit: ranks 2h and 2h + 1 serve row tile h of the
+// pair.  A 128 x 512 fp32 output accumulator is the whole of an SM's TMEM
+// (128 lanes x 512 columns), so one SM cannot hold Q, the scores S and O for
+// 128 rows; the two CTAs of a row tile split the work by role:
 //
-//   CTA rank 0 ("S"): Q's 512 no-PE dims live in TMEM (256 columns of packed
+//   even rank ("S"): Q's 512 no-PE dims live in TMEM (256 columns of packed
 //     bf16, the A operand of S = Q K^T from tensor memory), its 64 RoPE dims
 //     in shared memory; a 128-key tile of K arrives by TMA gather4 as three
 //     rounds of three 16 KB column chunks (a ring of one tile); two
@@ -21,7 +23,7 @@
 //     write P (bf16) to a local staging slot and ship each 64-key half to
 //     the partner with one bulk copy whose bytes complete the partner's
 //     barrier.
-//   CTA rank 1 ("O"): the fp32 O accumulator fills its TMEM; V (the first
+//   odd rank ("O"): the fp32 O accumulator fills its TMEM; V (the first
 //     512 dims of the same rows) arrives by TMA gather4 in 64-key x 256-dim
 //     half tiles; P halves land in four double-buffered slots;
 //     O += P V runs as N = 256 MMAs with both operands in shared memory.
@@ -30,9 +32,12 @@
 // (M128 N256 K16): 576 and 512 MACs per (row, key), balanced.
 //
 // Gathers are the throughput limit of this design (a TMA gather4 moves
-// 512 B, and one warp issues them one at a time, lane after lane), so each
-// CTA runs 16 producer warps in two teams that take turns round by round,
-// and setmaxnreg moves registers from the producer warpgroups to the
+// 512 B, and one warp issues them one at a time, lane after lane).  The two
+// S CTAs need the same K tiles and the two O CTAs the same V tiles, so each
+// gathers half of every tile and multicasts it into both; a ring slot is
+// reused once both consumers' MMAs have released it (tensor-core commits
+// multicast to both).  Each CTA runs 16 producer warps that share every
+// round, and setmaxnreg moves registers from the producer warpgroups to the
 // softmax / row warpgroups.
 //
 // Online softmax with a lazy maximum: O is rescaled only when a row's
@@ -65,8 +70,8 @@ constexpr int KEYS_S = 128;                // keys per S tile (N of the score MM
 constexpr int KEYS_O = 64;                 // keys per O tile (one P half)
 constexpr int THREADS = 896;               // 28 warps = 7 warpgroups
 constexpr int SOFTMAX_THREADS = 256;       // S: warps 0-7 (warpgroups 0, 1)
-constexpr int PRODUCER_WARP0 = 8;          // both: warps 8-23 (warpgroups 2-5) issue the TMA gathers,
-constexpr int TEAM_WARPS = 8;              //   two teams of 8 warps taking turns by round
+constexpr int PRODUCER_WARP0 = 8;          // both: warps 8-23 (warpgroups 2-5) issue the TMA gathers
+constexpr int PRODUCER_WARPS = 16;
 constexpr int MMA_WARP = 24;               // both: warpgroup 6; lane 0 of warp 24 issues the MMAs
 constexpr int LAUNCH_REGS = 72;            // registers per thread at launch: 65536 / 896, rounded down to 8
 constexpr int REGS_WIDE = 128;             // softmax and O-row warpgroups after setmaxnreg
@@ -100,6 +105,8 @@ constexpr uint32_t SMEM_ALLOC = SMEM_USED + 1024;    // room to align the base t
 static_assert(SMEM_ALLOC <= 232448, "at most 227 KB of shared memory per CTA");
 static_assert(S_RING % 1024 == 0 && O_VRING % 1024 == 0 && PSLOT % 1024 == 0, "swizzle atoms are 1 KB aligned");
 
+constexpr uint16_t S_MASK = 0x5;                      // the two S CTAs (ranks 0, 2)
+constexpr uint16_t O_MASK = 0xA;                      // the two O CTAs (ranks 1, 3)
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t TM_S0 = 256;                      // S role: S buffers at columns 256 and 384
 constexpr uint32_t IDESC_S = idesc_bf16(128, 128, false);
@@ -113,19 +120,19 @@ constexpr uint64_t TIMEOUT_NS = 1000000000ull;
 // so a barrier or field can be addressed in the partner with mapa.
 struct Header {
     uint64_t c_full[NKR];      // S: K round landed (8 producer-warp arrives + TMA bytes)
-    uint64_t c_empty[NKR];     // S: the MMAs reading the round completed (commit)
+    uint64_t c_empty[NKR];     // S: the MMAs of both S CTAs reading the round completed (2 multicast commits)
     uint64_t s_full[2];        // S: scores ready (commit) + valid-key bits copied (MMA thread)
     uint64_t s_free[2];        // S: the 8 softmax warps have read the score buffer
     uint64_t p_empty[2][2];    // S: the partner's P V MMAs on P slot [group][parity] completed (its commit)
     uint64_t v_full[NVH];      // O: V half tile landed (8 producer-warp arrives + TMA bytes)
-    uint64_t v_empty[NVH];     // O: the MMAs reading it completed
+    uint64_t v_empty[NVH];     // O: the MMAs of both O CTAs reading it completed (2 multicast commits)
     uint64_t p_full[2][2];     // O: P slot landed (the MMA thread's expect-tx arrive + bulk-copy bytes)
     uint64_t pv_sync;          // O: every MMA issued so far completed (before a rescale)
     uint64_t rs_req;           // O: MMA thread asks the row warps to rescale O (or to finish)
     uint64_t rs_done;          // O: the 4 row warps rescaled their rows
     uint64_t l_ready;          // O: the partner's 4 group-0 warps wrote 1/l
     uint64_t drain;            // both: all MMAs of the CTA completed
-    uint64_t t_valid[2][2];    // S: bit n of an S tile's 128 keys = key n has a valid slot (tile ring of 2)
+    uint16_t t_valid[2][8];    // S: byte w (producer warp w): bit k = key 4w + k, bit 4 + k = key 64 + 4w + k is valid (tile ring of 2)
     uint64_t s_valid[2][2];    // S: the same bits, per score buffer
     uint32_t tmem_base;
     uint32_t abort;
@@ -137,16 +144,16 @@ struct Header {
 static_assert(sizeof(Header) <= HEADER, "header fits");
 
 struct Unit {
-    int split, b;
+    int split, b, half;        // half: row tile of the pair (cluster rank >> 1)
     int64_t qo0, kv0, L, N, k0, k1, r0, rows_b;
     int ntiles;                // S tiles of 128 keys; the O CTA processes 2 * ntiles 64-key halves
-    int rot;                   // this pair starts at S tile `rot` of its split (see tile_key0)
+    int rot;                   // this unit starts at S tile `rot` of its split (see tile_key0)
 };
 
-// First key of the t-th S tile this pair processes.  The row tiles of one
+// First key of the t-th S tile this unit processes.  The units of one
 // request read the same keys; each starts at a different tile of the split
-// (rot = row tile * ntiles / row tiles) so they do not request the same rows
-// from L2 at the same moment.  Softmax order does not change the result.
+// (rot = pair * ntiles / pairs) so they do not request the same rows from L2
+// at the same moment.  Softmax order does not change the result.
 __device__ __forceinline__ int64_t tile_key0(const Unit &u, int t)
 {
     int s = t + u.rot;
@@ -258,50 +265,48 @@ __device__ __forceinline__ Slots resolve_slots(const Params &p, const RawSlots &
 // column block, 16-B pieces swizzled q -> q ^ (n & 7) inside each 1 KB group
 // of 8 keys (the tensor map's 128-byte swizzle): the K-major B operand of
 // the score MMAs.  A tile arrives as three rounds of three chunks; round g
-// of tile t goes to ring slot g and is issued by team (t + g) & 1.  Team
-// warp w owns keys 16w..16w+15 of each tile: lanes 0-3 each gather four
-// keys, one TMA gather4 per chunk of the round.  Both teams resolve the
-// slots of every tile.
+// of tile t goes to ring slot g.  Producer warp w (0-15) resolves key
+// groups w and w + 16 (four keys each) of every tile and, in the S CTA of
+// row tile h, gathers group w + 16h: one TMA gather4 per chunk of every
+// round, multicast to both S CTAs.  (A warp issues its TMA instructions one
+// after another, so each warp issues only three per round.)
 __device__ void s_gather(const Params &p, Header *h, const CUtensorMap *tmap, uint32_t smem, const Unit &u)
 {
-    const int pwa = (int)(threadIdx.x >> 5) - PRODUCER_WARP0;
-    const int team = pwa / TEAM_WARPS, pw = pwa % TEAM_WARPS;
+    const int pw = (int)(threadIdx.x >> 5) - PRODUCER_WARP0;
     const int lane = threadIdx.x & 31;
-    const bool act = lane < 4;
-    const int koff = pw * 16 + lane * 4;
-    RawSlots raw = load_slots(p, u, tile_key0(u, 0) + koff, act);
+    const bool act = lane < 2;
+    const int kg = pw + 16 * lane;                 // lane 0: group pw (keys 0-63), lane 1: group pw + 16
+    const bool issuer = act && lane == u.half;
+    RawSlots raw = load_slots(p, u, tile_key0(u, 0) + kg * 4, act);
     Slots cur = resolve_slots(p, raw);
-    if (u.ntiles > 1) raw = load_slots(p, u, tile_key0(u, 1) + koff, act);
+    if (u.ntiles > 1) raw = load_slots(p, u, tile_key0(u, 1) + kg * 4, act);
     bool ok = true;
     for (int t = 0; t < u.ntiles && ok; ++t) {
-        uint32_t bits16 = 0;
-#pragma unroll
-        for (int l = 0; l < 4; ++l) bits16 |= __shfl_sync(0xffffffffu, cur.nib, l) << (4 * l);
-#pragma unroll
+        const uint32_t bits8 = __shfl_sync(0xffffffffu, cur.nib, 0) | (__shfl_sync(0xffffffffu, cur.nib, 1) << 4);
+#pragma unroll 1
         for (int g = 0; g < NKR; ++g) {
-            if (((t + g) & 1) != team) continue;
             if (t > 0 && !__all_sync(0xffffffffu, wait_bar(h, smem_u32(&h->c_empty[g]), (uint32_t)(t - 1) & 1u, p.status))) {
                 ok = false;
                 break;
             }
             const uint32_t bar = smem_u32(&h->c_full[g]);
             if (lane == 0) {
-                if (g == 0) reinterpret_cast<volatile uint16_t *>(&h->t_valid[t & 1][0])[pw] = (uint16_t)bits16;
-                if (pw == 0) mbar_arrive_expect_tx(bar, KROUND);
+                if (g == 0) reinterpret_cast<volatile uint8_t *>(&h->t_valid[t & 1][0])[pw] = (uint8_t)bits8;
+                if (pw == 0) mbar_arrive_expect_tx(bar, KROUND);   // both halves land here
                 else mbar_arrive(bar);
             }
-            if (act) {
-                const uint32_t dst = smem + S_RING + (uint32_t)g * KROUND + (uint32_t)(pw * 4 + lane) * 512u;
+            if (issuer) {
+                const uint32_t dst = smem + S_RING + (uint32_t)g * KROUND + (uint32_t)kg * 512u;
 #pragma unroll
                 for (int cc = 0; cc < RCHUNKS; ++cc)
-                    tma_gather4(dst + (uint32_t)cc * KCHUNK, tmap, (g * RCHUNKS + cc) * 64, cur.y[0], cur.y[1], cur.y[2],
-                                cur.y[3], bar);
+                    tma_gather4_multicast(dst + (uint32_t)cc * KCHUNK, tmap, (g * RCHUNKS + cc) * 64, cur.y[0], cur.y[1],
+                                          cur.y[2], cur.y[3], bar, S_MASK);
             }
         }
         if (!ok) break;
         if (t + 1 < u.ntiles) {
             cur = resolve_slots(p, raw);                        // loaded one tile ago
-            if (t + 2 < u.ntiles) raw = load_slots(p, u, tile_key0(u, t + 2) + koff, act);
+            if (t + 2 < u.ntiles) raw = load_slots(p, u, tile_key0(u, t + 2) + kg * 4, act);
         }
     }
     // Every round issued was consumed, unless a wait timed out: then give
@@ -325,10 +330,18 @@ __device__ void s_mma(const Params &p, Header *h, uint32_t smem, uint32_t tmem, 
             if (!wait_bar(h, smem_u32(&h->c_full[g]), (uint32_t)t & 1u, p.status)) { ok = false; break; }
             tc_fence_after_sync();
             if (g == 0) {
-                volatile uint64_t *src = &h->t_valid[t & 1][0];
+                // valid bits in key order: byte w = key groups w (low nibble) and w + 16 (high nibble)
+                const volatile uint8_t *src = reinterpret_cast<const volatile uint8_t *>(&h->t_valid[t & 1][0]);
+                uint64_t w0 = 0, w1 = 0;
+#pragma unroll
+                for (int w = 0; w < 16; ++w) {
+                    const uint64_t v = src[w];
+                    w0 |= (v & 0xFull) << (4 * w);
+                    w1 |= ((v >> 4) & 0xFull) << (4 * w);
+                }
                 volatile uint64_t *dst = &h->s_valid[buf][0];
-                dst[0] = src[0];
-                dst[1] = src[1];
+                dst[0] = w0;
+                dst[1] = w1;
             }
 #pragma unroll
             for (int cc = 0; cc < RCHUNKS; ++cc) {
@@ -347,7 +360,7 @@ __device__ void s_mma(const Params &p, Header *h, uint32_t smem, uint32_t tmem, 
                                sdesc_sw128(sb + 32u * (uint32_t)k, 16u, 1024u), IDESC_S, 1u);
                 }
             }
-            mma_commit(smem_u32(&h->c_empty[g]));
+            mma_commit_multicast(smem_u32(&h->c_empty[g]), S_MASK);   // both S CTAs may refill the slot
         }
         if (!ok) break;
         mma_commit(smem_u32(&h->s_full[buf]));
@@ -448,6 +461,7 @@ __device__ void s_softmax(const Params &p, Header *h, uint32_t smem, uint32_t tm
     uint8_t *prow = stage + (r >> 3) * 1024 + (r & 7) * 128;
     const uint32_t stage_u32 = smem + S_STAGE + (uint32_t)grp * PSLOT;
     const uint32_t copy_bytes = grp == 0 ? PTILE + SIDE_BYTES : PTILE;
+    const uint32_t partner = 2u * (uint32_t)u.half + 1u;   // the O CTA of this row tile
     float *xmax = reinterpret_cast<float *>(reinterpret_cast<uint8_t *>(h) + S_XMAX);
     float m_used = -INFINITY, l = 0.f;
     bool ok = true;
@@ -478,17 +492,19 @@ __device__ void s_softmax(const Params &p, Header *h, uint32_t smem, uint32_t tm
         const bool all_vis = __all_sync(0xffffffffu, vis == ~0ull);
         const uint32_t v0 = (uint32_t)vis, v1 = (uint32_t)(vis >> 32);
 
-        float lmax = -INFINITY;
+        float mx4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};   // independent chains
         if (all_vis) {
 #pragma unroll
-            for (int n = 0; n < 32; ++n) lmax = fmaxf(lmax, fmaxf(__uint_as_float(sa[n]), __uint_as_float(sb[n])));
+            for (int n = 0; n < 32; ++n) mx4[n & 3] = fmaxf(mx4[n & 3], fmaxf(__uint_as_float(sa[n]), __uint_as_float(sb[n])));
         } else {
 #pragma unroll
             for (int n = 0; n < 32; ++n) {
-                lmax = fmaxf(lmax, ((v0 >> n) & 1u) ? __uint_as_float(sa[n]) : -INFINITY);
-                lmax = fmaxf(lmax, ((v1 >> n) & 1u) ? __uint_as_float(sb[n]) : -INFINITY);
+                const float a = ((v0 >> n) & 1u) ? __uint_as_float(sa[n]) : -INFINITY;
+                const float b = ((v1 >> n) & 1u) ? __uint_as_float(sb[n]) : -INFINITY;
+                mx4[n & 3] = fmaxf(mx4[n & 3], fmaxf(a, b));
             }
         }
+        const float lmax = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3]));
         xmax[(buf * 2 + grp) * ROWS + r] = lmax;
         // The staging slot is free once the previous bulk copy has read it.
         if (leader) bulk_wait_read_all();
@@ -507,7 +523,7 @@ __device__ void s_softmax(const Params &p, Header *h, uint32_t smem, uint32_t tm
 
         // p = 2^(s * sl2 - m_used) for this group's 64 keys; masked keys give 0.
         const float neg_m = m_used == -INFINITY ? 0.f : -m_used;
-        float psum = 0.f;
+        float ps4[4] = {0.f, 0.f, 0.f, 0.f};   // independent chains
 #pragma unroll
         for (int part = 0; part < 2; ++part) {
             const uint32_t *sv = part ? sb : sa;
@@ -521,7 +537,7 @@ __device__ void s_softmax(const Params &p, Header *h, uint32_t smem, uint32_t tm
                     p0 = ((vq >> (2 * n)) & 1u) ? p0 : 0.f;
                     p1 = ((vq >> (2 * n + 1)) & 1u) ? p1 : 0.f;
                 }
-                psum += p0 + p1;
+                ps4[n & 3] += p0 + p1;
                 pk[n] = pack_bf16x2(p0, p1);
             }
             // keys 32*part .. +31 of this half: 16-B pieces 4*part .. 4*part+3 of row r
@@ -530,7 +546,7 @@ __device__ void s_softmax(const Params &p, Header *h, uint32_t smem, uint32_t tm
                 *reinterpret_cast<uint4 *>(prow + ((((uint32_t)(4 * part + qq)) ^ (uint32_t)(r & 7)) << 4)) =
                     make_uint4(pk[4 * qq], pk[4 * qq + 1], pk[4 * qq + 2], pk[4 * qq + 3]);
         }
-        l += psum;
+        l += (ps4[0] + ps4[1]) + (ps4[2] + ps4[3]);
         if (grp == 0) {
             // The first half's O tile rescales O; the second half follows with the same maximum.
             reinterpret_cast<float *>(stage + PTILE)[r] = rescale ? alpha : 1.f;
@@ -545,8 +561,8 @@ __device__ void s_softmax(const Params &p, Header *h, uint32_t smem, uint32_t tm
         // Both groups vote here too, so they always leave the loop together.
         if (!named_barrier_and(6, SOFTMAX_THREADS, slot_free)) { ok = false; break; }
         if (leader) {
-            bulk_copy_to_cluster(map_cluster(smem + O_PSLOT + (uint32_t)(2 * grp + buf) * PSLOT, 1), stage_u32,
-                                 copy_bytes, map_cluster(smem_u32(&h->p_full[grp][buf]), 1));
+            bulk_copy_to_cluster(map_cluster(smem + O_PSLOT + (uint32_t)(2 * grp + buf) * PSLOT, partner), stage_u32,
+                                 copy_bytes, map_cluster(smem_u32(&h->p_full[grp][buf]), partner));
             bulk_commit_group();
         }
         // mask bits of tile t + 1 (loaded during this tile), then the loads for t + 2
@@ -565,49 +581,56 @@ __device__ void s_softmax(const Params &p, Header *h, uint32_t smem, uint32_t tm
         if (row < p.rows_cap)
             p.part_lse[(int64_t)u.split * p.rows_cap + row] = l > 0.f ? (m_used + log2f(l)) * LN2 : -INFINITY;
     }
-    st_cluster_f32(map_cluster(smem_u32(&h->inv_l[r]), 1), l > 0.f ? 1.f / l : 0.f);
+    st_cluster_f32(map_cluster(smem_u32(&h->inv_l[r]), partner), l > 0.f ? 1.f / l : 0.f);
     __syncwarp();
-    if (lane == 0) mbar_arrive_cluster(smem_u32(&h->l_ready), 1);
+    if (lane == 0) mbar_arrive_cluster(smem_u32(&h->l_ready), partner);
 }
 
 // ------------------------------------------------------------------ O role: gather (warps 8-23)
 //
 // V half tile layout: four 64-dim column blocks of 64 keys (8 KB each, key
 // rows of 128 B swizzled as above): the MN-major B operand of one N = 256
-// P V MMA.  Round R = 2 * (O tile) + half goes to ring slot R % 4; team k
-// issues the rounds of half k.  Team warp w, lane l (0-3) gathers key group
-// (4w + l) / 2 (four keys) for column blocks 2 (l & 1) and 2 (l & 1) + 1.
+// P V MMA.  Round R = 2 * (O tile) + value half goes to ring slot R % 4.
+// In the O CTA of row tile h, producer warp w gathers key group 8h + (w & 7)
+// (four keys of the 64), column blocks 2 (w >> 3) and 2 (w >> 3) + 1 of
+// every round, multicast to both O CTAs.
 __device__ void o_gather(const Params &p, Header *h, const CUtensorMap *tmap, uint32_t smem, const Unit &u)
 {
-    const int pwa = (int)(threadIdx.x >> 5) - PRODUCER_WARP0;
-    const int team = pwa / TEAM_WARPS, pw = pwa % TEAM_WARPS;
+    const int pw = (int)(threadIdx.x >> 5) - PRODUCER_WARP0;
     const int lane = threadIdx.x & 31;
-    const bool act = lane < 4;
-    const int kg = (pw * 4 + lane) >> 1, blk0 = (lane & 1) * 2;
+    const bool act = lane == 0;
+    const int kg = 8 * u.half + (pw & 7), blk0 = 2 * (pw >> 3);
     const int nt = 2 * u.ntiles;
     auto key0 = [&](int ot) { return tile_key0(u, ot >> 1) + (int64_t)(ot & 1) * KEYS_O + kg * 4; };
     RawSlots raw = load_slots(p, u, key0(0), act);
     Slots cur = resolve_slots(p, raw);
     raw = load_slots(p, u, key0(1), act);
     bool ok = true;
-    for (int ot = 0; ot < nt; ++ot) {
-        const int R = 2 * ot + team, slot = R % NVH, use = R / NVH;
-        if (use > 0 && !__all_sync(0xffffffffu, wait_bar(h, smem_u32(&h->v_empty[slot]), (uint32_t)(use - 1) & 1u, p.status))) {
-            ok = false;
-            break;
-        }
-        const uint32_t bar = smem_u32(&h->v_full[slot]);
-        if (lane == 0) {
-            if (pw == 0) mbar_arrive_expect_tx(bar, VHALF);
-            else mbar_arrive(bar);
-        }
-        if (act) {
-            const uint32_t dst = smem + O_VRING + (uint32_t)slot * VHALF + (uint32_t)kg * 512u;
+    int slot = 0;
+    uint32_t phase = 0;
+    for (int ot = 0; ot < nt && ok; ++ot) {
+#pragma unroll 1
+        for (int hf = 0; hf < 2; ++hf) {
+            const int R = 2 * ot + hf;
+            if (R >= NVH && !__all_sync(0xffffffffu, wait_bar(h, smem_u32(&h->v_empty[slot]), phase ^ 1u, p.status))) {
+                ok = false;
+                break;
+            }
+            const uint32_t bar = smem_u32(&h->v_full[slot]);
+            if (lane == 0) {
+                if (pw == 0) mbar_arrive_expect_tx(bar, VHALF);   // both O CTAs' key groups land here
+                else mbar_arrive(bar);
+            }
+            if (act) {
+                const uint32_t dst = smem + O_VRING + (uint32_t)slot * VHALF + (uint32_t)kg * 512u;
 #pragma unroll
-            for (int j = 0; j < 2; ++j)
-                tma_gather4(dst + (uint32_t)(blk0 + j) * VCHUNK, tmap, (4 * team + blk0 + j) * 64, cur.y[0], cur.y[1],
-                            cur.y[2], cur.y[3], bar);
+                for (int j = 0; j < 2; ++j)
+                    tma_gather4_multicast(dst + (uint32_t)(blk0 + j) * VCHUNK, tmap, (4 * hf + blk0 + j) * 64, cur.y[0],
+                                          cur.y[1], cur.y[2], cur.y[3], bar, O_MASK);
+            }
+            if (++slot == NVH) { slot = 0; phase ^= 1u; }
         }
+        if (!ok) break;
         if (ot + 1 < nt) {
             cur = resolve_slots(p, raw);
             if (ot + 2 < nt) raw = load_slots(p, u, key0(ot + 2), act);
@@ -654,11 +677,11 @@ __device__ void o_mma(const Params &p, Header *h, uint32_t smem, uint32_t tmem, 
             for (int k = 0; k < KEYS_O / 16; ++k)
                 mma_ss(tmem + 256u * (uint32_t)hf, sdesc_sw128(pb + 32u * (uint32_t)k, 16u, 1024u),
                        sdesc_sw128(vb + (uint32_t)k * 16u * 128u, VCHUNK, 1024u), IDESC_PV, (ot | k) ? 1u : 0u);
-            mma_commit(smem_u32(&h->v_empty[slot]));
+            mma_commit_multicast(smem_u32(&h->v_empty[slot]), O_MASK);   // both O CTAs may refill the slot
             if (++slot == NVH) { slot = 0; phase ^= 1u; }
         }
         if (!ok) break;
-        mma_commit_multicast(smem_u32(&h->p_empty[g][par]), (uint16_t)0x1);
+        mma_commit_multicast(smem_u32(&h->p_empty[g][par]), (uint16_t)(1u << (2 * u.half)));   // this row tile's S CTA
         // arm this slot for its next P transfer
         mbar_arrive_expect_tx(smem_u32(&h->p_full[g][par]), g == 0 ? PTILE + SIDE_BYTES : PTILE);
     }
@@ -719,23 +742,27 @@ __device__ void o_rows(const Params &p, Header *h, uint32_t smem, uint32_t tmem,
     }
 }
 
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
+__global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(THREADS, 1)
     tc_split_kernel(Params p, const __grid_constant__ CUtensorMap pool_map)
 {
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t smem = (raw + 1023u) & ~1023u;
     Header *h = reinterpret_cast<Header *>(smem_raw + (smem - raw));
-    const uint32_t role = cluster_rank();
+    const uint32_t rank = cluster_rank();
+    const uint32_t role = rank & 1u;        // 0: S, 1: O
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
-    // Segment decode.  Both CTAs of the pair compute the same unit, so they
-    // leave together when it is empty.  Grid: x = 2 * row tile + rank in
-    // the pair, y = split, z = request; row tiles vary fastest, so pairs
-    // that read the same key chunk run together and share it through L2.
+    // Segment decode.  All four CTAs of the cluster compute the same unit, so
+    // they leave together when it is empty.  Grid: x = 4 * pair of row tiles
+    // + rank, y = split, z = request; pairs vary fastest, so clusters that
+    // read the same key chunk run together and share it through L2.  The
+    // second row tile of a pair may be past the request's rows: its CTAs
+    // still take part (their gathers feed the first row tile) on zero rows.
     Unit u;
     u.split = (int)blockIdx.y;
     u.b = (int)blockIdx.z;
+    u.half = (int)(rank >> 1);
     u.qo0 = p.qo_indptr[u.b];
     const int64_t T = p.qo_indptr[u.b + 1] - u.qo0;
     u.kv0 = p.kv_indptr[u.b];
@@ -745,8 +772,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
         if (T < 0 || u.L < 0) return;
     }
     u.rows_b = (T < p.max_q_per_req ? T : p.max_q_per_req) * p.num_heads;
-    u.r0 = (int64_t)(blockIdx.x >> 1) * ROWS;
-    if (u.r0 >= u.rows_b) return;
+    const int64_t pair = blockIdx.x >> 2;
+    if (2 * pair * ROWS >= u.rows_b) return;
+    u.r0 = (2 * pair + u.half) * ROWS;
     u.N = u.L + T;
     const int64_t chunk = split_chunk(u.N, p.num_splits);
     u.k0 = (int64_t)u.split * chunk;
@@ -754,18 +782,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
     u.k1 = (u.k0 + chunk < u.N) ? u.k0 + chunk : u.N;
     u.ntiles = (int)((u.k1 - u.k0 + KEYS_S - 1) / KEYS_S);
     {
-        const int64_t row_tiles = (u.rows_b + ROWS - 1) / ROWS;
-        u.rot = (int)(((int64_t)(blockIdx.x >> 1) * u.ntiles) / row_tiles);
+        const int64_t pairs = (u.rows_b + 2 * ROWS - 1) / (2 * ROWS);
+        u.rot = (int)((pair * u.ntiles) / pairs);
     }
 
     if (tid == 0) {
         for (int s = 0; s < NKR; ++s) {
-            mbar_init(smem_u32(&h->c_full[s]), TEAM_WARPS);
-            mbar_init(smem_u32(&h->c_empty[s]), 1);
+            mbar_init(smem_u32(&h->c_full[s]), PRODUCER_WARPS);
+            mbar_init(smem_u32(&h->c_empty[s]), 2);
         }
         for (int s = 0; s < NVH; ++s) {
-            mbar_init(smem_u32(&h->v_full[s]), TEAM_WARPS);
-            mbar_init(smem_u32(&h->v_empty[s]), 1);
+            mbar_init(smem_u32(&h->v_full[s]), PRODUCER_WARPS);
+            mbar_init(smem_u32(&h->v_empty[s]), 2);
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(smem_u32(&h->s_full[i]), 2);
@@ -881,8 +909,8 @@ cudaError_t launch_tc_split(const Params &p, cudaStream_t stream)
 {
     CUtensorMap map;
     if (!encode_pool_map(p, &map)) return cudaErrorInvalidValue;
-    const int row_tiles = (int)((p.max_q_per_req * (int64_t)p.num_heads + ROWS - 1) / ROWS);
-    dim3 grid(2u * (unsigned)row_tiles, (unsigned)p.num_splits, (unsigned)p.batch);
+    const int pairs = (int)((p.max_q_per_req * (int64_t)p.num_heads + 2 * ROWS - 1) / (2 * ROWS));
+    dim3 grid(4u * (unsigned)pairs, (unsigned)p.num_splits, (unsigned)p.batch);
     tc_split_kernel<<<grid, THREADS, SMEM_ALLOC, stream>>>(p, map);
     return cudaGetLastError();
 }

@@ -12,13 +12,15 @@ import math
 from typing import Sequence
 
 NUM_SMS = 152                  # GB300: 2 dies x 76 SMs
+TC_CLUSTERS = 36               # 4-CTA clusters of the tensor-core kernel resident at once on a GB300
+                               # (a cluster stays inside one GPC: 144 of the 152 SMs)
 KEY_ALIGN = 128                # must match the library's split chunk rule
 MIN_CHUNK = 256
-CANDIDATES = (1, 2, 3, 4, 5, 6, 7, 8, 10, 12, 14, 16, 20, 24, 28, 32, 40, 48, 56, 64, 80, 96, 128, 160, 192, 256)
+CANDIDATES = tuple(range(1, 65)) + (72, 80, 96, 108, 128, 144, 160, 192, 256)
 
 
 def split_chunk(n: int, num_splits: int) -> int:
-    """Keys per split: max(ceil(n / S), 256) rounded up to 64 (the library's rule)."""
+    """Keys per split: max(ceil(n / S), 256) rounded up to 128 (the library's rule)."""
     c = max(-(-n // num_splits), MIN_CHUNK)
     return -(-c // KEY_ALIGN) * KEY_ALIGN
 
@@ -29,18 +31,19 @@ def splits_used(n: int, num_splits: int) -> int:
 
 def simulate(prefix_lens: Sequence[int], draft_lens: Sequence[int], num_heads: int, num_splits: int,
              kernel: str = "tc") -> float:
-    """Estimated time of one call in units of one 64-key tile of a 128-row unit.
+    """Estimated time of one call in units of one key tile of a unit.
 
-    Units are dispatched in grid order (row tile fastest, then split, then
-    request) onto the concurrent slots (76 CTA pairs for the tensor-core
-    kernel, 304 CTAs for the CUDA-core one); each costs its key tiles plus a
-    fixed start-up (query tile load, pipeline fill, partial write).  The
-    combine's workspace traffic is added on top.
+    Units are dispatched in grid order (row group fastest, then split, then
+    request) onto the concurrent slots (36 four-CTA clusters of 256 rows for
+    the tensor-core kernel, 128-key tiles; 304 CTAs of 16 rows for the
+    CUDA-core one, 32-key tiles); each costs its key tiles plus a fixed
+    start-up (query load, pipeline fill, partial write).  The combine's
+    workspace traffic is added on top.
     """
     if kernel == "simt":
-        rows, slots, overhead, tile_keys, tile_cost = 16, 2 * NUM_SMS, 2.0, 32, 1.0
+        rows, slots, overhead, tile_keys, tile_cost, tile_s = 16, 2 * NUM_SMS, 2.0, 32, 1.0, 0.5e-6
     else:
-        rows, slots, overhead, tile_keys, tile_cost = 128, NUM_SMS // 2, 8.0, 64, 1.0
+        rows, slots, overhead, tile_keys, tile_cost, tile_s = 256, TC_CLUSTERS, 4.0, 128, 1.0, 2.5e-6
     max_q = max(draft_lens) if len(draft_lens) else 0
     max_tiles = math.ceil(max_q * num_heads / rows)
     free = [0.0] * slots
@@ -60,9 +63,8 @@ def simulate(prefix_lens: Sequence[int], draft_lens: Sequence[int], num_heads: i
                 t0 = heapq.heappop(free)
                 heapq.heappush(free, t0 + cost)
                 finish = max(finish, t0 + cost)
-    # combine: each used split's fp32 partial row (2 KB) written then read at ~6.8 TB/s,
-    # against ~0.56 us per tile unit
-    combine = total_rows_splits * 2048 * 2 / 6.8e12 / 0.56e-6
+    # combine: each used split's fp32 partial row (2 KB) written then read at ~6.8 TB/s
+    combine = total_rows_splits * 2048 * 2 / 6.8e12 / tile_s
     return finish + combine
 
 
