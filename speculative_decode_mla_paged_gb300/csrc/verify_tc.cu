@@ -147,18 +147,15 @@ struct Unit {
     int split, b, half;        // half: row tile of the pair (cluster rank >> 1)
     int64_t qo0, kv0, L, N, k0, k1, r0, rows_b;
     int ntiles;                // S tiles of 128 keys; the O CTA processes 2 * ntiles 64-key halves
-    int rot;                   // this unit starts at S tile `rot` of its split (see tile_key0)
 };
 
-// First key of the t-th S tile this unit processes.  The units of one
-// request read the same keys; each starts at a different tile of the split
-// (rot = pair * ntiles / pairs) so they do not request the same rows from L2
-// at the same moment.  Softmax order does not change the result.
+// First key of the t-th S tile of a unit.  The units of one split of a
+// request (its pairs of row tiles) walk the same tiles in the same order,
+// run together (pairs are the fastest grid index) and so share each tile
+// through L2 instead of re-reading it from DRAM.
 __device__ __forceinline__ int64_t tile_key0(const Unit &u, int t)
 {
-    int s = t + u.rot;
-    if (s >= u.ntiles) s -= u.ntiles;
-    return u.k0 + (int64_t)s * KEYS_S;
+    return u.k0 + (int64_t)t * KEYS_S;
 }
 
 // ------------------------------------------------------------------ bounded waits
@@ -781,10 +778,6 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(THREADS, 1)
     if (u.k0 >= u.N) return;
     u.k1 = (u.k0 + chunk < u.N) ? u.k0 + chunk : u.N;
     u.ntiles = (int)((u.k1 - u.k0 + KEYS_S - 1) / KEYS_S);
-    {
-        const int64_t pairs = (u.rows_b + 2 * ROWS - 1) / (2 * ROWS);
-        u.rot = (int)((pair * u.ntiles) / pairs);
-    }
 
     if (tid == 0) {
         for (int s = 0; s < NKR; ++s) {
