@@ -380,10 +380,11 @@ def run_ours(args):
         "clocks": clocks,
     }
 
-    # ---- the five workloads, device time per call (informational)
+    # ---- the five workloads and the two extra ones (chain verify, decode),
+    # device time per call (informational)
     if rank == 0 and not args.no_per_config:
         table = {}
-        for name in W.CONFIG_ORDER:
+        for name in W.CONFIG_ORDER + W.EXTRA_CONFIG_ORDER:
             ci = inp if name == args.config else W.make_config_inputs(name, device=dev)
             cs = args.num_splits or default_splits(name, ci, args.kernel)
             cd = d if name == args.config else device_tensors(ci, torch, dev)

@@ -233,6 +233,54 @@ VERIFY_ATTN_API int verify_attn_run_static(const void *q, int64_t q_stride_tok, 
                                            int batch, int max_q_per_req, int num_heads, int num_splits,
                                            verify_attn_stream_t stream);
 
+/*
+ * KV save of the draft tokens ("The Launch Wrapper", section The KV Cache
+ * Ordering Insight: the new tokens' latent rows are written into the pool
+ * before the attention reads them):
+ *     kv_pool[out_cache_loc[i], :] = kv_new[i, :]   for i in [0, num_tokens).
+ *
+ *   kv_new        [num_tokens, 576] bf16; row i at kv_new + i*kv_new_stride_tok
+ *                 (elements, a multiple of 8, >= 576); 16-B aligned base.
+ *   out_cache_loc [num_tokens] int64 destination slots.  Slots are expected
+ *                 to be distinct (which write lands for a repeated slot is
+ *                 unspecified); a slot outside [0, pool_size) is skipped and
+ *                 sets VA_STATUS_BAD_SLOT.
+ *   kv_pool       [pool_size, 576] bf16, written in place; 16-B aligned.
+ *   workspace     at least 256 bytes, 256-B aligned: the status word at byte
+ *                 0 is cleared, then set by the kernel (read it after a sync).
+ *
+ * One launch on `stream`; allocates nothing, does not synchronise.  Returns
+ * VA_OK, VA_ERR_NULL, VA_ERR_ALIGN, VA_ERR_DIMS (num_tokens < 0 or
+ * pool_size <= 0), VA_ERR_WORKSPACE, VA_ERR_DEVICE or VA_ERR_LAUNCH.
+ */
+VERIFY_ATTN_API int verify_attn_save_kv(const void *kv_new, int64_t kv_new_stride_tok,
+                                        const int64_t *out_cache_loc, int64_t num_tokens,
+                                        void *kv_pool, int64_t pool_size,
+                                        void *workspace, size_t workspace_bytes,
+                                        verify_attn_stream_t stream);
+
+/*
+ * The KV save of the draft tokens, then verify_attn_run, on `stream`: the
+ * save kernel writes rows [0, qo_indptr[batch]) of kv_new ([sum T_b, 576]
+ * bf16, row stride kv_new_stride_tok elements, a multiple of 8, >= 576) to
+ * kv_pool at out_cache_loc, and the attention that follows reads them.  The
+ * save grid covers batch * max_q_per_req rows and reads the real count from
+ * qo_indptr on the device, so one captured graph serves every batch within
+ * the capacities.  The status word collects the save's and the attention's
+ * bits.  Other arguments and return codes are those of verify_attn_run.
+ */
+VERIFY_ATTN_API int verify_attn_save_and_run(const void *kv_new, int64_t kv_new_stride_tok,
+                                             const void *q, int64_t q_stride_tok, int64_t q_stride_head,
+                                             void *kv_pool, int64_t pool_size,
+                                             const int32_t *qo_indptr, const int32_t *kv_indptr,
+                                             const int32_t *kv_indices, const int64_t *out_cache_loc,
+                                             const uint8_t *custom_mask, const int64_t *mask_indptr,
+                                             float sm_scale,
+                                             void *out, int64_t out_stride_tok, int64_t out_stride_head,
+                                             int batch, int max_q_per_req, int num_heads, int num_splits,
+                                             void *workspace, size_t workspace_bytes,
+                                             verify_attn_stream_t stream);
+
 /* Short English description of a VA_* status code (static storage). */
 VERIFY_ATTN_API const char *verify_attn_status_string(int status);
 

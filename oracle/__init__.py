@@ -117,3 +117,18 @@ def run(inp, rows=None, num_splits=0):
     return verify_attn(inp.q, inp.kv_pool, inp.qo_indptr, inp.kv_indptr, inp.kv_indices,
                        inp.out_cache_loc, inp.custom_mask, inp.mask_indptr, inp.sm_scale,
                        inp.num_heads, rows=rows, num_splits=num_splits)
+
+
+def save_kv(kv_pool_bits: np.ndarray, out_cache_loc: np.ndarray, kv_new_bits: np.ndarray) -> np.ndarray:
+    """The KV save step ("The Launch Wrapper", section The KV Cache Ordering
+    Insight): a copy of the pool (bf16 bit patterns, [pool_size, 576] uint16)
+    with row out_cache_loc[i] replaced by kv_new[i] for every i.  Slots must
+    be distinct and inside the pool (the definition has no other case)."""
+    pool = np.array(kv_pool_bits, dtype=np.uint16, copy=True)
+    loc = np.asarray(out_cache_loc, dtype=np.int64)
+    if loc.size and (loc.min() < 0 or loc.max() >= pool.shape[0]):
+        raise ValueError("slot outside the pool")
+    if len(np.unique(loc)) != loc.size:
+        raise ValueError("slots must be distinct")
+    pool[loc] = np.asarray(kv_new_bits, dtype=np.uint16).reshape(loc.size, -1)
+    return pool

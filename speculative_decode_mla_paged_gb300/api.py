@@ -11,6 +11,7 @@ import ctypes
 import os
 import re
 import threading
+import warnings
 from typing import Optional
 
 import torch
@@ -59,6 +60,10 @@ def load_library():
                 fn.restype = _i32
             lib.verify_attn_run_profiled.argtypes = [_i32, _p] + _RUN_ARGS
             lib.verify_attn_run_profiled.restype = _i32
+            lib.verify_attn_save_kv.argtypes = [_p, _i64, _p, _i64, _p, _i64, _p, ctypes.c_size_t, _p]
+            lib.verify_attn_save_kv.restype = _i32
+            lib.verify_attn_save_and_run.argtypes = [_p, _i64] + _RUN_ARGS
+            lib.verify_attn_save_and_run.restype = _i32
             lib.verify_attn_status_string.argtypes = [_i32]
             lib.verify_attn_status_string.restype = ctypes.c_char_p
             _lib = lib
@@ -104,7 +109,7 @@ def verify_attn(q: torch.Tensor, kv_pool: torch.Tensor, qo_indptr: torch.Tensor,
                 custom_mask: torch.Tensor, mask_indptr: torch.Tensor, sm_scale: float, *,
                 out: torch.Tensor, workspace: torch.Tensor, max_q_per_req: int, num_splits: int,
                 impl: str = "tc", stream: Optional[torch.cuda.Stream] = None,
-                events=None) -> torch.Tensor:
+                events=None, kv_new: Optional[torch.Tensor] = None) -> torch.Tensor:
     """Tree-verify attention into ``out`` ([sum T_b, H, 512] bf16).
 
     Tensors are used in place (no copies): q [sum T_b, H, 576] bf16 with a
@@ -115,6 +120,10 @@ def verify_attn(q: torch.Tensor, kv_pool: torch.Tensor, qo_indptr: torch.Tensor,
     ``events``: optional four torch.cuda.Event objects recorded at the start
     of the call, before the split kernel, between it and the combine, and
     after the combine.
+    ``kv_new``: optional [sum T_b, 576] bf16 rows of the draft tokens; when
+    given, the library first writes them into ``kv_pool`` at
+    ``out_cache_loc`` (the KV save) and the attention reads them
+    (verify_attn_save_and_run; production kernel only, no events).
     """
     lib = load_library()
     _check_dev("q", q, torch.bfloat16)
@@ -140,7 +149,14 @@ def verify_attn(q: torch.Tensor, kv_pool: torch.Tensor, qo_indptr: torch.Tensor,
     s = stream if stream is not None else torch.cuda.current_stream(q.device)
     if impl not in ("tc", "simt"):
         raise ValueError(f"unknown impl {impl!r}")
-    if events is not None:
+    if kv_new is not None:
+        _check_dev("kv_new", kv_new, torch.bfloat16)
+        if kv_new.dim() != 2 or kv_new.shape[1] != LATENT_DIM or kv_new.stride(1) != 1 or kv_new.shape[0] < q.shape[0]:
+            raise ValueError("kv_new must be [>= tokens, 576] with a contiguous last dim")
+        if impl != "tc" or events is not None:
+            raise ValueError("kv_new runs with the production kernel and without events")
+        fn = lambda *a: lib.verify_attn_save_and_run(_ptr(kv_new), kv_new.stride(0), *a)
+    elif events is not None:
         for e in events:                 # torch creates the CUDA event lazily, on first record
             if e is not None and not e.cuda_event:
                 e.record(s)
@@ -158,6 +174,30 @@ def verify_attn(q: torch.Tensor, kv_pool: torch.Tensor, qo_indptr: torch.Tensor,
     return out
 
 
+def save_kv(kv_new: torch.Tensor, out_cache_loc: torch.Tensor, kv_pool: torch.Tensor, workspace: torch.Tensor,
+            stream: Optional[torch.cuda.Stream] = None) -> None:
+    """The KV save alone: kv_pool[out_cache_loc[i]] = kv_new[i] (in place).
+    ``workspace``: a uint8 CUDA tensor of at least 256 bytes; its status word
+    reports slots outside the pool (``read_status``)."""
+    lib = load_library()
+    _check_dev("kv_new", kv_new, torch.bfloat16)
+    _check_dev("kv_pool", kv_pool, torch.bfloat16)
+    _check_dev("out_cache_loc", out_cache_loc, torch.int64)
+    _check_dev("workspace", workspace, torch.uint8)
+    if kv_new.dim() != 2 or kv_new.shape[1] != LATENT_DIM or kv_new.stride(1) != 1:
+        raise ValueError("kv_new must be [tokens, 576] with a contiguous last dim")
+    if kv_pool.dim() != 2 or kv_pool.shape[1] != LATENT_DIM or not kv_pool.is_contiguous():
+        raise ValueError("kv_pool must be a contiguous [pool_size, 576] tensor")
+    if not out_cache_loc.is_contiguous() or out_cache_loc.numel() != kv_new.shape[0]:
+        raise ValueError("out_cache_loc must be contiguous with one slot per kv_new row")
+    s = stream if stream is not None else torch.cuda.current_stream(kv_pool.device)
+    rc = lib.verify_attn_save_kv(_ptr(kv_new), kv_new.stride(0), _ptr(out_cache_loc), kv_new.shape[0],
+                                 _ptr(kv_pool), kv_pool.shape[0], _ptr(workspace), workspace.numel(),
+                                 ctypes.c_void_p(s.cuda_stream))
+    if rc != 0:
+        raise VerifyAttnError(f"verify_attn_save_kv: {status_string(rc)} ({rc})")
+
+
 def read_status(workspace: torch.Tensor) -> int:
     """The device status word (byte 0 of the workspace); synchronises the device."""
     return int(workspace[:4].view(torch.int32).item()) & 0xFFFFFFFF
@@ -169,24 +209,64 @@ class VerifyAttention:
     Allocate once (before any CUDA-graph capture), then call repeatedly --
     "The Capture-Safe Kernel", Decision 4 (workspace as a caller tensor) and
     Decision 3 (grid fixed by host capacities).
+
+    Validate mode (``validate=True``, or the environment variable
+    VERIFY_ATTN_VALIDATE=1): every call also runs the other kernel ("simt"
+    for "tc" and the reverse) on the same live buffers into a scratch
+    output, compares the two (|a - b| <= atol + rtol |b| per element), keeps
+    the figures in ``last_validation`` and warns on a mismatch; the caller
+    still receives the primary kernel's output.  This is the offline analogue
+    of the pages' validate mode ("The Launch Wrapper", section The Design
+    Decision: Three Modes of Operation).  It synchronises, so it is for eager
+    runs, not for graph capture.
     """
 
     def __init__(self, batch: int, max_q_per_req: int, num_heads: int, num_splits: int,
-                 device="cuda", impl: str = "tc"):
+                 device="cuda", impl: str = "tc", validate: Optional[bool] = None,
+                 atol: float = 1e-2, rtol: float = 1e-2):
         self.batch, self.max_q_per_req = batch, max_q_per_req
         self.num_heads, self.num_splits, self.impl = num_heads, num_splits, impl
+        if validate is None:
+            validate = os.environ.get("VERIFY_ATTN_VALIDATE", "0") == "1"
+        self.validate, self.atol, self.rtol = bool(validate), float(atol), float(rtol)
+        self.last_validation = None
         init()
         self.workspace = torch.empty(workspace_size(batch, max_q_per_req, num_heads, num_splits),
                                      dtype=torch.uint8, device=device)
+        self._check_ws = None
 
     def __call__(self, q, kv_pool, qo_indptr, kv_indptr, kv_indices, out_cache_loc, custom_mask,
-                 mask_indptr, sm_scale, out, stream=None, events=None):
+                 mask_indptr, sm_scale, out, stream=None, events=None, kv_new=None):
         if qo_indptr.numel() - 1 > self.batch:
             raise ValueError("batch exceeds the workspace capacity")
-        return verify_attn(q, kv_pool, qo_indptr, kv_indptr, kv_indices, out_cache_loc, custom_mask,
-                           mask_indptr, sm_scale, out=out, workspace=self.workspace,
-                           max_q_per_req=self.max_q_per_req, num_splits=self.num_splits,
-                           impl=self.impl, stream=stream, events=events)
+        res = verify_attn(q, kv_pool, qo_indptr, kv_indptr, kv_indices, out_cache_loc, custom_mask,
+                          mask_indptr, sm_scale, out=out, workspace=self.workspace,
+                          max_q_per_req=self.max_q_per_req, num_splits=self.num_splits,
+                          impl=self.impl, stream=stream, events=events, kv_new=kv_new)
+        if self.validate:
+            self._cross_check(q, kv_pool, qo_indptr, kv_indptr, kv_indices, out_cache_loc, custom_mask,
+                              mask_indptr, sm_scale, out, stream)
+        return res
+
+    def _cross_check(self, q, kv_pool, qo_indptr, kv_indptr, kv_indices, out_cache_loc, custom_mask,
+                     mask_indptr, sm_scale, out, stream):
+        if self._check_ws is None:
+            self._check_ws = torch.empty_like(self.workspace)
+        other = "simt" if self.impl == "tc" else "tc"
+        ref = torch.empty_like(out)
+        verify_attn(q, kv_pool, qo_indptr, kv_indptr, kv_indices, out_cache_loc, custom_mask, mask_indptr,
+                    sm_scale, out=ref, workspace=self._check_ws, max_q_per_req=self.max_q_per_req,
+                    num_splits=self.num_splits, impl=other, stream=stream)
+        a, b = out.float(), ref.float()
+        diff = (a - b).abs()
+        excess = diff - (self.atol + self.rtol * b.abs())
+        rec = {"against": other, "max_abs_diff": float(diff.max()) if diff.numel() else 0.0,
+               "max_excess": float(excess.max()) if excess.numel() else float("-inf"),
+               "status": read_status(self.workspace), "check_status": read_status(self._check_ws)}
+        rec["ok"] = bool(rec["max_excess"] <= 0 and rec["status"] == 0 and rec["check_status"] == 0)
+        self.last_validation = rec
+        if not rec["ok"]:
+            warnings.warn(f"verify-attn validate: {self.impl} vs {other}: {rec}")
 
     def status(self) -> int:
         return read_status(self.workspace)

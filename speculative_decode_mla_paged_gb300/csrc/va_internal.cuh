@@ -76,5 +76,8 @@ __device__ inline int64_t key_slot(const Params &p, int64_t kv0, int64_t qo0, in
 cudaError_t simt_init();
 cudaError_t launch_simt_split(const Params &p, cudaStream_t stream);
 cudaError_t launch_combine(const Params &p, cudaStream_t stream);
+cudaError_t launch_kv_save(const __nv_bfloat16 *kv_new, int64_t stride_tok, const int64_t *out_cache_loc,
+                           int64_t cap, const int32_t *count, __nv_bfloat16 *kv_pool, int64_t pool_size,
+                           unsigned *status, cudaStream_t stream);
 
 }  // namespace va

@@ -99,18 +99,28 @@ int prepare(Params &p, const void *q, int64_t q_st, int64_t q_sh, const void *kv
 
 enum class Impl { Tc, Simt };
 
+// Draft rows to write into the pool before the attention (verify_attn_save_and_run).
+struct SaveArgs {
+    const void *kv_new;
+    int64_t stride_tok;
+};
+
 int run(Impl impl, const void *q, int64_t q_st, int64_t q_sh, const void *kv_pool,
         int64_t pool_size, const int32_t *qo_indptr, const int32_t *kv_indptr,
         const int32_t *kv_indices, const int64_t *out_cache_loc, const uint8_t *custom_mask,
         const int64_t *mask_indptr, float sm_scale, void *out, int64_t o_st, int64_t o_sh,
         int batch, int max_q, int heads, int splits, void *workspace, size_t ws_bytes,
-        verify_attn_stream_t stream, cudaEvent_t const *events = nullptr)
+        verify_attn_stream_t stream, cudaEvent_t const *events = nullptr, const SaveArgs *save = nullptr)
 {
     Params p;
     int rc = prepare(p, q, q_st, q_sh, kv_pool, pool_size, qo_indptr, kv_indptr, kv_indices,
                      out_cache_loc, custom_mask, mask_indptr, sm_scale, out, o_st, o_sh, batch,
                      max_q, heads, splits, workspace, ws_bytes);
     if (rc != VA_OK) return rc;
+    if (save != nullptr) {
+        if (save->kv_new == nullptr || out_cache_loc == nullptr) return VA_ERR_NULL;
+        if (!aligned(save->kv_new, 16) || (save->stride_tok & 7) || save->stride_tok < D) return VA_ERR_ALIGN;
+    }
     rc = ensure_init();
     if (rc != VA_OK) return rc;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
@@ -119,6 +129,11 @@ int run(Impl impl, const void *q, int64_t q_st, int64_t q_sh, const void *kv_poo
     };
     if (!mark(0)) return VA_ERR_LAUNCH;
     if (cudaMemsetAsync(p.status, 0, sizeof(unsigned), s) != cudaSuccess) return VA_ERR_LAUNCH;
+    if (save != nullptr &&
+        launch_kv_save(static_cast<const __nv_bfloat16 *>(save->kv_new), save->stride_tok, out_cache_loc,
+                       (int64_t)batch * max_q, qo_indptr + batch, const_cast<__nv_bfloat16 *>(p.kv_pool), pool_size,
+                       p.status, s) != cudaSuccess)
+        return VA_ERR_LAUNCH;
     if (!mark(1)) return VA_ERR_LAUNCH;
     cudaError_t e = cudaSuccess;
     if (p.rows_cap > 0) {
@@ -190,6 +205,42 @@ int verify_attn_run_profiled(int impl, void *const *events, const void *q, int64
                    out_cache_loc, custom_mask, mask_indptr, sm_scale, out, out_stride_tok,
                    out_stride_head, batch, max_q_per_req, num_heads, num_splits, workspace,
                    workspace_bytes, stream, reinterpret_cast<cudaEvent_t const *>(events));
+}
+
+int verify_attn_save_kv(const void *kv_new, int64_t kv_new_stride_tok, const int64_t *out_cache_loc,
+                        int64_t num_tokens, void *kv_pool, int64_t pool_size, void *workspace,
+                        size_t workspace_bytes, verify_attn_stream_t stream)
+{
+    if (num_tokens < 0 || pool_size <= 0) return VA_ERR_DIMS;
+    if (!kv_pool || !workspace || (num_tokens > 0 && (!kv_new || !out_cache_loc))) return VA_ERR_NULL;
+    if (!va::aligned(kv_pool, 16) || !va::aligned(workspace, 256) ||
+        (num_tokens > 0 && (!va::aligned(kv_new, 16) || (kv_new_stride_tok & 7) || kv_new_stride_tok < va::D)))
+        return VA_ERR_ALIGN;
+    if (workspace_bytes < va::WS_HEADER) return VA_ERR_WORKSPACE;
+    const int rc = va::ensure_init();
+    if (rc != VA_OK) return rc;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    unsigned *status = static_cast<unsigned *>(workspace);
+    if (cudaMemsetAsync(status, 0, sizeof(unsigned), s) != cudaSuccess) return VA_ERR_LAUNCH;
+    if (va::launch_kv_save(static_cast<const __nv_bfloat16 *>(kv_new), kv_new_stride_tok, out_cache_loc, num_tokens,
+                           nullptr, static_cast<__nv_bfloat16 *>(kv_pool), pool_size, status, s) != cudaSuccess)
+        return VA_ERR_LAUNCH;
+    return VA_OK;
+}
+
+int verify_attn_save_and_run(const void *kv_new, int64_t kv_new_stride_tok, const void *q, int64_t q_stride_tok,
+                             int64_t q_stride_head, void *kv_pool, int64_t pool_size, const int32_t *qo_indptr,
+                             const int32_t *kv_indptr, const int32_t *kv_indices, const int64_t *out_cache_loc,
+                             const uint8_t *custom_mask, const int64_t *mask_indptr, float sm_scale, void *out,
+                             int64_t out_stride_tok, int64_t out_stride_head, int batch, int max_q_per_req,
+                             int num_heads, int num_splits, void *workspace, size_t workspace_bytes,
+                             verify_attn_stream_t stream)
+{
+    const va::SaveArgs save{kv_new, kv_new_stride_tok};
+    return va::run(va::Impl::Tc, q, q_stride_tok, q_stride_head, kv_pool, pool_size, qo_indptr, kv_indptr,
+                   kv_indices, out_cache_loc, custom_mask, mask_indptr, sm_scale, out, out_stride_tok,
+                   out_stride_head, batch, max_q_per_req, num_heads, num_splits, workspace, workspace_bytes,
+                   stream, nullptr, &save);
 }
 
 const char *verify_attn_status_string(int status)

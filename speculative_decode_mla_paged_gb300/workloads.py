@@ -57,6 +57,7 @@ class VerifyConfig:
     ragged_prefix_range: Optional[tuple] = None  # (lo, hi) log-uniform, request 0 fixed at hi
     draft_choices: Optional[Sequence[int]] = None
     sm_scale: float = SM_SCALE
+    tree: str = "random"                      # draft tree shape: "random", "chain" or "star"
     description: str = ""
 
 
@@ -84,6 +85,19 @@ CONFIGS = {
                     "T in {16,32,64}, H=8, pool 1.5M"),
 }
 CONFIG_ORDER = ["tiny", "short", "mid", "long", "ragged"]
+
+# Second workloads on the same kernels (degenerate masks): a linear draft
+# (chain verify) and plain decode (one new token per request).
+CONFIGS["chain"] = VerifyConfig(
+    name="chain", prefix_lens=[23040] * 4, draft_lens=[32] * 4, num_heads=8, pool_size=131072, seed=5,
+    batch=4, tree="chain",
+    description="B=4, prefix 23040 each, T=32 linear draft (chain verify), H=8, pool 131072")
+CONFIGS["decode"] = VerifyConfig(
+    name="decode", prefix_lens=None, draft_lens=[1] * 32, num_heads=16, pool_size=1_000_000, seed=6,
+    batch=32, ragged_prefix_range=(1024, 32768),
+    description="B=32, prefix log-uniform [1024,32768] with request 0 at 32768, T=1 (decode), H=16, "
+                "pool 1M")
+EXTRA_CONFIG_ORDER = ["chain", "decode"]
 
 
 @dataclasses.dataclass
@@ -290,4 +304,4 @@ def make_config_inputs(name: str, device="cpu") -> VerifyInputs:
     rng = np.random.Generator(np.random.PCG64(cfg.seed + 7919))
     prefix, drafts = draw_lengths(cfg, rng)
     return make_inputs(prefix, drafts, cfg.num_heads, cfg.pool_size, cfg.seed,
-                       q_scale=cfg.q_scale, sm_scale=cfg.sm_scale, device=device, cfg_name=name)
+                       q_scale=cfg.q_scale, sm_scale=cfg.sm_scale, device=device, tree=cfg.tree, cfg_name=name)

@@ -44,6 +44,21 @@ def test_large_configs_sampled_rows(name, splits, impl):
     assert_parity(got[rows], oracle_rows(inp_host, rows), f"{name}/{impl}")
 
 
+@pytest.mark.parametrize("impl", IMPLS)
+@pytest.mark.parametrize("name", ["chain", "decode"])
+def test_extra_workloads(name, impl):
+    """Chain verify (linear draft) and plain decode (T = 1) on the same
+    kernels: sampled rows against the oracle, all rows finite."""
+    inp = W.make_config_inputs(name, device="cuda")
+    out, status = run(inp, impl=impl, num_splits=9)
+    assert status == 0
+    got = as_rows(out)
+    assert np.all(np.isfinite(got))
+    inp.q, inp.kv_pool = inp.q.cpu(), inp.kv_pool.cpu()
+    rows = sample_rows(inp, n_random=48, seed=7)
+    assert_parity(got[rows], oracle_rows(inp, rows), f"{name}/{impl}")
+
+
 def test_large_config_kernels_agree_on_every_row():
     """At full size every row of the tensor-core path matches the CUDA-core
     path within the same bar (the oracle covers the sampled rows above)."""

@@ -328,3 +328,23 @@ def test_bad_slot_and_bad_mask_indptr_are_errors():
         oracle.verify_attn(inp.q, inp.kv_pool, inp.qo_indptr, inp.kv_indptr, inp.kv_indices,
                            inp.out_cache_loc, inp.custom_mask, inp.mask_indptr + np.array([0, 1]),
                            inp.sm_scale, 1)
+
+
+def test_save_kv_oracle_replaces_exactly_the_named_rows():
+    """The KV save definition: named rows replaced, every other row untouched,
+    invalid or repeated slots rejected."""
+    rng = np.random.default_rng(3)
+    pool = rng.integers(0, 1 << 16, size=(50, 576), dtype=np.uint16)
+    loc = np.array([7, 0, 49, 23], dtype=np.int64)
+    new = rng.integers(0, 1 << 16, size=(4, 576), dtype=np.uint16)
+    pool0 = pool.copy()
+    got = oracle.save_kv(pool, loc, new)
+    for i, s in enumerate(loc):
+        assert np.array_equal(got[s], new[i])
+    others = np.setdiff1d(np.arange(50), loc)
+    assert np.array_equal(got[others], pool[others])
+    assert np.array_equal(pool, pool0)                   # the input is not modified in place
+    with pytest.raises(ValueError):
+        oracle.save_kv(pool, np.array([1, 1]), new[:2])
+    with pytest.raises(ValueError):
+        oracle.save_kv(pool, np.array([50]), new[:1])
