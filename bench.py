@@ -155,6 +155,22 @@ def dist_setup(args):
     return world, rank, local
 
 
+def max_over_ranks(value, world, device=None):
+    """The largest of the ranks' values: the job takes as long as its slowest
+    replica.  With one rank, the value itself (no process group needed)."""
+    import torch
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    if world > 1:
+        import torch.distributed as dist
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def per_call_us(total_ms, steps, world):
+    """Whole-job time per call: every rank ran `steps` calls in `total_ms`."""
+    return total_ms * 1e3 / (steps * world)
+
+
 # ------------------------------------------------------------------ oracle (CPU) timing
 
 def visible_per_row(inp):
@@ -311,11 +327,8 @@ def run_ours(args):
     status = runner.status()
     if status != 0:
         raise RuntimeError(f"device status word {status:#x}")
-    total = torch.tensor([sum(call_ms)], dtype=torch.float64, device=dev)
-    if world > 1:
-        dist.all_reduce(total, op=dist.ReduceOp.MAX)
-    t_total_ms = float(total.item())
-    value_us = t_total_ms * 1e3 / (args.steps * world)
+    t_total_ms = max_over_ranks(sum(call_ms), world, dev)
+    value_us = per_call_us(t_total_ms, args.steps, world)
 
     # ---- end-to-end: pinned host inputs -> device, call, result -> host
     h2d_names = ("q", "qo_indptr", "kv_indptr", "kv_indices", "out_cache_loc", "custom_mask", "mask_indptr")
@@ -338,10 +351,7 @@ def run_ours(args):
         e1.synchronize()
         if k >= args.warmup:
             e2e_ms.append(e0.elapsed_time(e1))
-    e2e_total = torch.tensor([sum(e2e_ms)], dtype=torch.float64, device=dev)
-    if world > 1:
-        dist.all_reduce(e2e_total, op=dist.ReduceOp.MAX)
-    e2e_us = float(e2e_total.item()) * 1e3 / (args.steps * world)
+    e2e_us = per_call_us(max_over_ranks(sum(e2e_ms), world, dev), args.steps, world)
 
     # ---- roofline of the dominant kernel (the split kernel)
     flops = inp.algorithmic_flops()
