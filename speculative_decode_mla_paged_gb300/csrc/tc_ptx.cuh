@@ -215,6 +215,18 @@ __device__ __forceinline__ void tma_gather4_multicast(uint32_t dst, const void *
         : "memory");
 }
 
+// A plain tile (box as the map says) at coordinates (x, y), multicast like
+// tma_gather4_multicast.
+__device__ __forceinline__ void tma_tile_multicast(uint32_t dst, const void *tmap, int x, int y, uint32_t bar,
+                                                   uint16_t cta_mask)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.multicast::cluster "
+        "[%0], [%1, {%2, %3}], [%4], %5;"
+        ::"r"(dst), "l"(reinterpret_cast<uint64_t>(tmap)), "r"(x), "r"(y), "r"(bar), "h"(cta_mask)
+        : "memory");
+}
+
 __device__ __forceinline__ void prefetch_tensormap(const void *tmap)
 {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(tmap)) : "memory");

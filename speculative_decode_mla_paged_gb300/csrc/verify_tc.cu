@@ -256,6 +256,28 @@ __device__ __forceinline__ Slots resolve_slots(const Params &p, const RawSlots &
     return o;
 }
 
+// Slot of key j of the unit's request (-1 for a missing index buffer).
+__device__ __forceinline__ int64_t slot_of(const Params &p, const Unit &u, int64_t j)
+{
+    if (j < u.L) return p.kv_indices ? (int64_t)__ldg(p.kv_indices + u.kv0 + j) : -1;
+    return p.out_cache_loc ? __ldg(p.out_cache_loc + u.qo0 + (j - u.L)) : -1;
+}
+
+// True when every key of the unit, [k0, k1), sits in consecutive valid pool
+// slots (a defragmented pool).  Called by all 512 producer threads of a CTA:
+// the slots of the first and last key decide at once for every thread alike
+// (so a fragmented pool costs two cached loads and no barrier); only if they
+// line up do the threads check every consecutive pair and vote once.
+__device__ bool unit_contiguous(const Params &p, const Unit &u, int pt)
+{
+    const int64_t first = slot_of(p, u, u.k0), last = slot_of(p, u, u.k1 - 1);
+    if (first < 0 || last >= p.pool_size || last - first != u.k1 - 1 - u.k0) return false;
+    bool ok = true;
+#pragma unroll 1
+    for (int64_t j = u.k0 + 1 + pt; j < u.k1; j += PRODUCER_WARPS * 32) ok &= slot_of(p, u, j) == slot_of(p, u, j - 1) + 1;
+    return named_barrier_and(7, PRODUCER_WARPS * 32, ok);
+}
+
 // ------------------------------------------------------------------ S role: gather (warps 8-23)
 //
 // K chunk layout: 128 keys as 128-B rows (key n at n*128) of one 64-dim
@@ -267,7 +289,14 @@ __device__ __forceinline__ Slots resolve_slots(const Params &p, const RawSlots &
 // row tile h, gathers group w + 16h: one TMA gather4 per chunk of every
 // round, multicast to both S CTAs.  (A warp issues its TMA instructions one
 // after another, so each warp issues only three per round.)
-__device__ void s_gather(const Params &p, Header *h, const CUtensorMap *tmap, uint32_t smem, const Unit &u)
+//
+// Contiguous fast path: when all the unit's keys sit in consecutive pool
+// slots (a defragmented pool; decided once per unit), one lane loads each
+// chunk of a full tile with a single plain TMA tile of this CTA's 64 rows
+// (run_map: box 64 x 64) instead of 16 gather4s.  A partial last tile is
+// gathered, so no row past the unit's last key is read.
+__device__ void s_gather(const Params &p, Header *h, const CUtensorMap *tmap, const CUtensorMap *run_map,
+                         uint32_t smem, const Unit &u)
 {
     const int pw = (int)(threadIdx.x >> 5) - PRODUCER_WARP0;
     const int lane = threadIdx.x & 31;
@@ -277,9 +306,12 @@ __device__ void s_gather(const Params &p, Header *h, const CUtensorMap *tmap, ui
     RawSlots raw = load_slots(p, u, tile_key0(u, 0) + kg * 4, act);
     Slots cur = resolve_slots(p, raw);
     if (u.ntiles > 1) raw = load_slots(p, u, tile_key0(u, 1) + kg * 4, act);
+    const bool contiguous = unit_contiguous(p, u, pw * 32 + lane);
     bool ok = true;
     for (int t = 0; t < u.ntiles && ok; ++t) {
         const uint32_t bits8 = __shfl_sync(0xffffffffu, cur.nib, 0) | (__shfl_sync(0xffffffffu, cur.nib, 1) << 4);
+        const bool run = contiguous && tile_key0(u, t) + KEYS_S <= u.k1;
+        const int base = cur.y[0];                       // warp 0's issuer lane: the first key of this CTA's 64
 #pragma unroll 1
         for (int g = 0; g < NKR; ++g) {
             if (t > 0 && !__all_sync(0xffffffffu, wait_bar(h, smem_u32(&h->c_empty[g]), (uint32_t)(t - 1) & 1u, p.status))) {
@@ -292,7 +324,15 @@ __device__ void s_gather(const Params &p, Header *h, const CUtensorMap *tmap, ui
                 if (pw == 0) mbar_arrive_expect_tx(bar, KROUND);   // both halves land here
                 else mbar_arrive(bar);
             }
-            if (issuer) {
+            if (run) {
+                if (pw == 0 && lane == u.half) {
+                    const uint32_t dst = smem + S_RING + (uint32_t)g * KROUND + (uint32_t)u.half * 64u * 128u;
+#pragma unroll
+                    for (int cc = 0; cc < RCHUNKS; ++cc)
+                        tma_tile_multicast(dst + (uint32_t)cc * KCHUNK, run_map, (g * RCHUNKS + cc) * 64, base, bar,
+                                           S_MASK);
+                }
+            } else if (issuer) {
                 const uint32_t dst = smem + S_RING + (uint32_t)g * KROUND + (uint32_t)kg * 512u;
 #pragma unroll
                 for (int cc = 0; cc < RCHUNKS; ++cc)
@@ -590,8 +630,11 @@ __device__ void s_softmax(const Params &p, Header *h, uint32_t smem, uint32_t tm
 // P V MMA.  Round R = 2 * (O tile) + value half goes to ring slot R % 4.
 // In the O CTA of row tile h, producer warp w gathers key group 8h + (w & 7)
 // (four keys of the 64), column blocks 2 (w >> 3) and 2 (w >> 3) + 1 of
-// every round, multicast to both O CTAs.
-__device__ void o_gather(const Params &p, Header *h, const CUtensorMap *tmap, uint32_t smem, const Unit &u)
+// every round, multicast to both O CTAs.  Contiguous fast path as for K
+// (decided once per unit, full O tiles only): one lane loads each column
+// block with a plain TMA tile of this CTA's 32 rows (run_map: box 64 x 32).
+__device__ void o_gather(const Params &p, Header *h, const CUtensorMap *tmap, const CUtensorMap *run_map,
+                         uint32_t smem, const Unit &u)
 {
     const int pw = (int)(threadIdx.x >> 5) - PRODUCER_WARP0;
     const int lane = threadIdx.x & 31;
@@ -602,10 +645,13 @@ __device__ void o_gather(const Params &p, Header *h, const CUtensorMap *tmap, ui
     RawSlots raw = load_slots(p, u, key0(0), act);
     Slots cur = resolve_slots(p, raw);
     raw = load_slots(p, u, key0(1), act);
+    const bool contiguous = unit_contiguous(p, u, pw * 32 + lane);
     bool ok = true;
     int slot = 0;
     uint32_t phase = 0;
     for (int ot = 0; ot < nt && ok; ++ot) {
+        const bool run = contiguous && key0(ot) - kg * 4 + KEYS_O <= u.k1;
+        const int base = cur.y[0];                       // warp 0, lane 0: the first key of this CTA's 32
 #pragma unroll 1
         for (int hf = 0; hf < 2; ++hf) {
             const int R = 2 * ot + hf;
@@ -618,7 +664,14 @@ __device__ void o_gather(const Params &p, Header *h, const CUtensorMap *tmap, ui
                 if (pw == 0) mbar_arrive_expect_tx(bar, VHALF);   // both O CTAs' key groups land here
                 else mbar_arrive(bar);
             }
-            if (act) {
+            if (run) {
+                if (pw == 0 && lane == 0) {
+                    const uint32_t dst = smem + O_VRING + (uint32_t)slot * VHALF + (uint32_t)u.half * 32u * 128u;
+#pragma unroll
+                    for (int blk = 0; blk < 4; ++blk)
+                        tma_tile_multicast(dst + (uint32_t)blk * VCHUNK, run_map, (4 * hf + blk) * 64, base, bar, O_MASK);
+                }
+            } else if (act) {
                 const uint32_t dst = smem + O_VRING + (uint32_t)slot * VHALF + (uint32_t)kg * 512u;
 #pragma unroll
                 for (int j = 0; j < 2; ++j)
@@ -740,7 +793,8 @@ __device__ void o_rows(const Params &p, Header *h, uint32_t smem, uint32_t tmem,
 }
 
 __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(THREADS, 1)
-    tc_split_kernel(Params p, const __grid_constant__ CUtensorMap pool_map)
+    tc_split_kernel(Params p, const __grid_constant__ CUtensorMap pool_map,
+                    const __grid_constant__ CUtensorMap run_map_k, const __grid_constant__ CUtensorMap run_map_v)
 {
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
@@ -809,7 +863,10 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(THREADS, 1)
                 for (int j = 0; j < 2; ++j)
                     mbar_arrive_expect_tx(smem_u32(&h->p_full[i][j]), i == 0 ? PTILE + SIDE_BYTES : PTILE);
     }
-    if (warp == PRODUCER_WARP0 && lane == 0) prefetch_tensormap(&pool_map);
+    if (warp == PRODUCER_WARP0 && lane == 0) {
+        prefetch_tensormap(&pool_map);
+        prefetch_tensormap(role == 0 ? &run_map_k : &run_map_v);
+    }
     if (warp == MMA_WARP) {
         tmem_alloc(smem_u32(&h->tmem_base), TMEM_COLS);
         tmem_relinquish();
@@ -832,8 +889,8 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(THREADS, 1)
     } else {
         regs_dec<REGS_NARROW>();
         if (warp >= PRODUCER_WARP0 && warp < MMA_WARP) {
-            if (role == 0) s_gather(p, h, &pool_map, smem, u);
-            else o_gather(p, h, &pool_map, smem, u);
+            if (role == 0) s_gather(p, h, &pool_map, &run_map_k, smem, u);
+            else o_gather(p, h, &pool_map, &run_map_v, smem, u);
         } else if (warp == MMA_WARP) {
             if (role == 0) {
                 named_barrier_sync(1, SOFTMAX_THREADS + 32);
@@ -861,13 +918,14 @@ PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 std::once_flag g_encode_once;
 
 // 2-D tensor map over the pool [pool_size rows, 576 bf16]: box of 64
-// columns x 1 row (the gather4 form), 128-byte swizzle, zero fill outside.
-bool encode_pool_map(const Params &p, CUtensorMap *map)
+// columns x `rows` rows (1 row: the gather4 form; 64 / 32 rows: the
+// contiguous fast path's tiles), 128-byte swizzle, zero fill outside.
+bool encode_pool_map(const Params &p, CUtensorMap *map, uint32_t rows = 1)
 {
     if (g_encode == nullptr || p.pool_size >= ((int64_t)1 << 31)) return false;
     const cuuint64_t dims[2] = {(cuuint64_t)D, (cuuint64_t)p.pool_size};
     const cuuint64_t strides[1] = {(cuuint64_t)D * sizeof(__nv_bfloat16)};
-    const cuuint32_t box[2] = {64, 1};
+    const cuuint32_t box[2] = {64, rows};
     const cuuint32_t estr[2] = {1, 1};
     return g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<__nv_bfloat16 *>(p.kv_pool), dims, strides,
                     box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -900,11 +958,12 @@ bool tc_supported(const Params &p) { return p.pool_size < ((int64_t)1 << 31); }
 
 cudaError_t launch_tc_split(const Params &p, cudaStream_t stream)
 {
-    CUtensorMap map;
-    if (!encode_pool_map(p, &map)) return cudaErrorInvalidValue;
+    CUtensorMap map, run_k, run_v;
+    if (!encode_pool_map(p, &map) || !encode_pool_map(p, &run_k, 64) || !encode_pool_map(p, &run_v, 32))
+        return cudaErrorInvalidValue;
     const int pairs = (int)((p.max_q_per_req * (int64_t)p.num_heads + 2 * ROWS - 1) / (2 * ROWS));
     dim3 grid(4u * (unsigned)pairs, (unsigned)p.num_splits, (unsigned)p.batch);
-    tc_split_kernel<<<grid, THREADS, SMEM_ALLOC, stream>>>(p, map);
+    tc_split_kernel<<<grid, THREADS, SMEM_ALLOC, stream>>>(p, map, run_k, run_v);
     return cudaGetLastError();
 }
 

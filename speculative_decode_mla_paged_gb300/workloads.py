@@ -58,6 +58,7 @@ class VerifyConfig:
     draft_choices: Optional[Sequence[int]] = None
     sm_scale: float = SM_SCALE
     tree: str = "random"                      # draft tree shape: "random", "chain" or "star"
+    slots: str = "random"                     # pool slot layout: "random", "contiguous" or "runs:<k>"
     description: str = ""
 
 
@@ -97,7 +98,12 @@ CONFIGS["decode"] = VerifyConfig(
     batch=32, ragged_prefix_range=(1024, 32768),
     description="B=32, prefix log-uniform [1024,32768] with request 0 at 32768, T=1 (decode), H=16, "
                 "pool 1M")
-EXTRA_CONFIG_ORDER = ["chain", "decode"]
+CONFIGS["contig"] = VerifyConfig(
+    name="contig", prefix_lens=[23040] * 4, draft_lens=[32] * 4, num_heads=8, pool_size=131072, seed=7,
+    batch=4, slots="contiguous",
+    description="B=4, prefix 23040 each, T=32 random trees, H=8, pool 131072, contiguous slots "
+                "(defragmented pool)")
+EXTRA_CONFIG_ORDER = ["chain", "decode", "contig"]
 
 
 @dataclasses.dataclass
@@ -253,13 +259,35 @@ def _float_inputs(shape_q, pool_shape, q_scale, seed, device, rng):
     return q.reshape(shape_q), pool.reshape(pool_shape)
 
 
+def slot_order(rng: np.random.Generator, pool_size: int, n_keys: int, slots: str) -> np.ndarray:
+    """The pool slots handed out in request order (prefix, then drafts).
+
+    "random": a random permutation of the pool (a fragmented pool);
+    "contiguous": one run starting at a random offset (a defragmented pool:
+    every request's keys sit in consecutive slots); "runs:<k>": the pool cut
+    into runs of k consecutive slots, the runs shuffled (partly fragmented).
+    """
+    if slots == "random":
+        return rng.permutation(pool_size).astype(np.int64)
+    if slots == "contiguous":
+        off = int(rng.integers(0, pool_size - n_keys + 1))
+        return (off + np.arange(pool_size, dtype=np.int64)) % pool_size
+    if slots.startswith("runs:"):
+        k = int(slots.split(":")[1])
+        starts = np.arange(0, pool_size, k, dtype=np.int64)
+        rng.shuffle(starts)
+        return np.concatenate([np.arange(s0, min(s0 + k, pool_size), dtype=np.int64) for s0 in starts])
+    raise ValueError(slots)
+
+
 def make_inputs(prefix_lens, draft_lens, num_heads, pool_size, seed, *, q_scale=1.0,
                 sm_scale=SM_SCALE, device="cpu", parents=None, tree="random",
-                extra_prefix_mask=None, cfg_name="custom") -> VerifyInputs:
+                extra_prefix_mask=None, cfg_name="custom", slots="random") -> VerifyInputs:
     """Draw one ragged batch.
 
     tree: "random" (parent uniform over root and earlier drafts), "chain"
     (parent[i] = i-1), or "star" (every draft hangs off the root).
+    slots: pool slot layout (see ``slot_order``).
     """
     rng = np.random.Generator(np.random.PCG64(seed))
     prefix_lens = np.asarray(prefix_lens, dtype=np.int64)
@@ -277,7 +305,7 @@ def make_inputs(prefix_lens, draft_lens, num_heads, pool_size, seed, *, q_scale=
     n_keys = int(prefix_lens.sum() + draft_lens.sum())
     if n_keys > pool_size:
         raise ValueError(f"pool of {pool_size} slots cannot hold {n_keys} tokens")
-    perm = rng.permutation(pool_size).astype(np.int64)
+    perm = slot_order(rng, pool_size, n_keys, slots)
     kv_idx, ocl = [], []
     off = 0
     for b in range(bsz):
@@ -304,4 +332,5 @@ def make_config_inputs(name: str, device="cpu") -> VerifyInputs:
     rng = np.random.Generator(np.random.PCG64(cfg.seed + 7919))
     prefix, drafts = draw_lengths(cfg, rng)
     return make_inputs(prefix, drafts, cfg.num_heads, cfg.pool_size, cfg.seed,
-                       q_scale=cfg.q_scale, sm_scale=cfg.sm_scale, device=device, tree=cfg.tree, cfg_name=name)
+                       q_scale=cfg.q_scale, sm_scale=cfg.sm_scale, device=device, tree=cfg.tree, cfg_name=name,
+                       slots=cfg.slots)

@@ -45,10 +45,11 @@ def test_large_configs_sampled_rows(name, splits, impl):
 
 
 @pytest.mark.parametrize("impl", IMPLS)
-@pytest.mark.parametrize("name", ["chain", "decode"])
+@pytest.mark.parametrize("name", ["chain", "decode", "contig"])
 def test_extra_workloads(name, impl):
-    """Chain verify (linear draft) and plain decode (T = 1) on the same
-    kernels: sampled rows against the oracle, all rows finite."""
+    """Chain verify (linear draft), plain decode (T = 1) and a defragmented
+    pool (contiguous slots: the tensor-core kernel's plain-tile fast path) on
+    the same kernels: sampled rows against the oracle, all rows finite."""
     inp = W.make_config_inputs(name, device="cuda")
     out, status = run(inp, impl=impl, num_splits=9)
     assert status == 0
@@ -57,6 +58,17 @@ def test_extra_workloads(name, impl):
     inp.q, inp.kv_pool = inp.q.cpu(), inp.kv_pool.cpu()
     rows = sample_rows(inp, n_random=48, seed=7)
     assert_parity(got[rows], oracle_rows(inp, rows), f"{name}/{impl}")
+
+
+@pytest.mark.parametrize("slots", ["runs:64", "runs:37", "runs:200", "contiguous"])
+def test_contiguous_runs_every_row(slots):
+    """Pools cut into runs of consecutive slots: some 64-key (K) and 32-key
+    (V) shares of a tile are contiguous and take plain TMA tiles, the others
+    gathers; every output row against the oracle."""
+    inp = W.make_inputs([3000, 1500, 700], [32, 16, 8], 8, 65536, seed=41, slots=slots)
+    out, status = run(inp, impl="tc", num_splits=3)
+    assert status == 0
+    assert_parity(as_rows(out), oracle_rows(inp), f"tc/{slots}")
 
 
 def test_large_config_kernels_agree_on_every_row():
