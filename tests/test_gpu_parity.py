@@ -71,6 +71,19 @@ def test_contiguous_runs_every_row(slots):
     assert_parity(as_rows(out), oracle_rows(inp), f"tc/{slots}")
 
 
+@pytest.mark.parametrize("impl", IMPLS)
+@pytest.mark.parametrize("sm_scale,q_scale", [(-0.3, 1.0), (0.0, 1.0), (2.5, 1.0), (W.SM_SCALE, 8.0)])
+def test_softmax_scale_and_range(sm_scale, q_scale, impl):
+    """Negative, zero and large softmax scales (the tensor-core kernel folds a
+    negative scale into Q's signs; a zero scale gives uniform weights over the
+    visible keys) and a wide score range (many online rescales): every row
+    against the oracle."""
+    inp = W.make_inputs([1500, 600], [24, 8], 8, 8192, seed=53, q_scale=q_scale, sm_scale=sm_scale)
+    out, status = run(inp, impl=impl, num_splits=2)
+    assert status == 0
+    assert_parity(as_rows(out), oracle_rows(inp), f"{impl}/scale={sm_scale}/q={q_scale}")
+
+
 def test_large_config_kernels_agree_on_every_row():
     """At full size every row of the tensor-core path matches the CUDA-core
     path within the same bar (the oracle covers the sampled rows above)."""
