@@ -6,10 +6,15 @@
 //   m* = max_s lse_s,  w_s = exp(lse_s - m*),  out = sum_s w_s O_s / sum_s w_s
 //
 // One warp per output row; each lane owns 16 of the 512 columns (four
-// float4 loads per split, fully coalesced).  Splits past the end of the
-// request are never read: their count follows from the indptrs with the
-// same chunk rule the split kernels use.  Output is bf16, round to nearest
-// even; a row whose splits all have lse = -inf (no visible key) gets zeros.
+// float4 loads per split, fully coalesced).  The lanes first read the
+// splits' lse values side by side (lane k: splits k, k + 32, ...) and agree
+// on the maximum and the weights with warp shuffles, so the loop over the
+// splits issues its partial loads without waiting on a weight and several
+// splits' loads are in flight at once; the sum still runs in split order.
+// Splits past the end of the request are never read: their count follows
+// from the indptrs with the same chunk rule the split kernels use.  Output
+// is bf16, round to nearest even; a row whose splits all have lse = -inf (no
+// visible key) gets zeros.
 #include "va_internal.cuh"
 
 #include <math.h>
@@ -41,28 +46,42 @@ __global__ void __launch_bounds__(WARPS * 32) combine_kernel(Params p)
     const int64_t ns = processed ? splits_used(L + T, p.num_splits) : 0;
 
     float m = -INFINITY;
-    for (int64_t s = 0; s < ns; ++s) m = fmaxf(m, p.part_lse[s * p.rows_cap + row]);
+    for (int64_t s = lane; s < ns; s += 32) m = fmaxf(m, p.part_lse[s * p.rows_cap + row]);
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
 
     float4 acc[4];
 #pragma unroll
     for (int j = 0; j < 4; ++j) acc[j] = make_float4(0.f, 0.f, 0.f, 0.f);
     float wsum = 0.f;
     if (m != -INFINITY) {
-        for (int64_t s = 0; s < ns; ++s) {
-            const float lse = p.part_lse[s * p.rows_cap + row];
-            if (lse == -INFINITY) continue;
-            const float w = expf(lse - m);
-            wsum += w;
-            const float4 *o = reinterpret_cast<const float4 *>(p.part_o + (s * p.rows_cap + row) * DV);
+        for (int64_t s0 = 0; s0 < ns; s0 += 32) {
+            // this lane's weight: split s0 + lane (0 past the end or with lse = -inf)
+            float wl = 0.f;
+            if (s0 + lane < ns) {
+                const float lse = p.part_lse[(s0 + lane) * p.rows_cap + row];
+                wl = lse == -INFINITY ? 0.f : expf(lse - m);
+            }
+            wsum += wl;
+            const int n = ns - s0 < 32 ? (int)(ns - s0) : 32;
+#pragma unroll 4
+            for (int k = 0; k < n; ++k) {
+                const float w = __shfl_sync(0xffffffffu, wl, k);
+                const float4 *o = reinterpret_cast<const float4 *>(p.part_o + ((s0 + k) * p.rows_cap + row) * DV);
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                const float4 v = o[j * 32 + lane];
-                acc[j].x = fmaf(w, v.x, acc[j].x);
-                acc[j].y = fmaf(w, v.y, acc[j].y);
-                acc[j].z = fmaf(w, v.z, acc[j].z);
-                acc[j].w = fmaf(w, v.w, acc[j].w);
+                for (int j = 0; j < 4; ++j) {
+                    const float4 v = o[j * 32 + lane];
+                    if (w != 0.f) {   // a split without visible keys adds nothing
+                        acc[j].x = fmaf(w, v.x, acc[j].x);
+                        acc[j].y = fmaf(w, v.y, acc[j].y);
+                        acc[j].z = fmaf(w, v.z, acc[j].z);
+                        acc[j].w = fmaf(w, v.w, acc[j].w);
+                    }
+                }
             }
         }
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) wsum += __shfl_xor_sync(0xffffffffu, wsum, off);
     }
     const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
     __nv_bfloat16 *dst = p.out + t * p.out_stride_tok + (int64_t)h * p.out_stride_head;
