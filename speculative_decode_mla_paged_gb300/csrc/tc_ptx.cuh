@@ -215,7 +215,16 @@ __device__ __forceinline__ void tma_gather4_multicast(uint32_t dst, const void *
         : "memory");
 }
 
-// A plain tile (box as the map says) at coordinates (x, y), multicast like
+// A plain tile (box as the map says) at coordinates (x, y) into this CTA.
+__device__ __forceinline__ void tma_tile(uint32_t dst, const void *tmap, int x, int y, uint32_t bar)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];"
+        ::"r"(dst), "l"(reinterpret_cast<uint64_t>(tmap)), "r"(x), "r"(y), "r"(bar)
+        : "memory");
+}
+
+// The same tile multicast like
 // tma_gather4_multicast.
 __device__ __forceinline__ void tma_tile_multicast(uint32_t dst, const void *tmap, int x, int y, uint32_t bar,
                                                    uint16_t cta_mask)

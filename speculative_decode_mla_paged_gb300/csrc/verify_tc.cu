@@ -105,8 +105,16 @@ constexpr uint32_t SMEM_ALLOC = SMEM_USED + 1024;    // room to align the base t
 static_assert(SMEM_ALLOC <= 232448, "at most 227 KB of shared memory per CTA");
 static_assert(S_RING % 1024 == 0 && O_VRING % 1024 == 0 && PSLOT % 1024 == 0, "swizzle atoms are 1 KB aligned");
 
-constexpr uint16_t S_MASK = 0x5;                      // the two S CTAs (ranks 0, 2)
-constexpr uint16_t O_MASK = 0xA;                      // the two O CTAs (ranks 1, 3)
+// Cluster shapes: NT row tiles of 128 rows per cluster, 2 * NT CTAs.  NT = 2
+// (the shape described above) for requests of more than 128 rows; NT = 1
+// (one S and one O CTA, each gathering whole tiles) when T * H <= 128, so a
+// short request does not hold two SMs for an empty row tile.
+template <int NT>
+struct Shape {
+    static_assert(NT == 1 || NT == 2, "one or two row tiles per cluster");
+    static constexpr uint16_t S_MASK = NT == 2 ? 0x5 : 0x1;   // the S CTAs (ranks 0, 2 / rank 0)
+    static constexpr uint16_t O_MASK = NT == 2 ? 0xA : 0x2;   // the O CTAs (ranks 1, 3 / rank 1)
+};
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t TM_S0 = 256;                      // S role: S buffers at columns 256 and 384
 constexpr uint32_t IDESC_S = idesc_bf16(128, 128, false);
@@ -144,7 +152,7 @@ struct Header {
 static_assert(sizeof(Header) <= HEADER, "header fits");
 
 struct Unit {
-    int split, b, half;        // half: row tile of the pair (cluster rank >> 1)
+    int split, b, half;        // half: row tile of the cluster (cluster rank >> 1)
     int64_t qo0, kv0, L, N, k0, k1, r0, rows_b;
     int ntiles;                // S tiles of 128 keys; the O CTA processes 2 * ntiles 64-key halves
 };
@@ -295,6 +303,7 @@ __device__ bool unit_contiguous(const Params &p, const Unit &u, int pt)
 // chunk of a full tile with a single plain TMA tile of this CTA's 64 rows
 // (run_map: box 64 x 64) instead of 16 gather4s.  A partial last tile is
 // gathered, so no row past the unit's last key is read.
+template <int NT>
 __device__ void s_gather(const Params &p, Header *h, const CUtensorMap *tmap, const CUtensorMap *run_map,
                          uint32_t smem, const Unit &u)
 {
@@ -302,7 +311,7 @@ __device__ void s_gather(const Params &p, Header *h, const CUtensorMap *tmap, co
     const int lane = threadIdx.x & 31;
     const bool act = lane < 2;
     const int kg = pw + 16 * lane;                 // lane 0: group pw (keys 0-63), lane 1: group pw + 16
-    const bool issuer = act && lane == u.half;
+    const bool issuer = act && (NT == 1 || lane == u.half);   // one S CTA: both lanes gather
     RawSlots raw = load_slots(p, u, tile_key0(u, 0) + kg * 4, act);
     Slots cur = resolve_slots(p, raw);
     if (u.ntiles > 1) raw = load_slots(p, u, tile_key0(u, 1) + kg * 4, act);
@@ -311,7 +320,7 @@ __device__ void s_gather(const Params &p, Header *h, const CUtensorMap *tmap, co
     for (int t = 0; t < u.ntiles && ok; ++t) {
         const uint32_t bits8 = __shfl_sync(0xffffffffu, cur.nib, 0) | (__shfl_sync(0xffffffffu, cur.nib, 1) << 4);
         const bool run = contiguous && tile_key0(u, t) + KEYS_S <= u.k1;
-        const int base = cur.y[0];                       // warp 0's issuer lane: the first key of this CTA's 64
+        const int base = cur.y[0];                       // warp 0, lane l: the slot of key 64 l
 #pragma unroll 1
         for (int g = 0; g < NKR; ++g) {
             if (t > 0 && !__all_sync(0xffffffffu, wait_bar(h, smem_u32(&h->c_empty[g]), (uint32_t)(t - 1) & 1u, p.status))) {
@@ -325,19 +334,28 @@ __device__ void s_gather(const Params &p, Header *h, const CUtensorMap *tmap, co
                 else mbar_arrive(bar);
             }
             if (run) {
-                if (pw == 0 && lane == u.half) {
-                    const uint32_t dst = smem + S_RING + (uint32_t)g * KROUND + (uint32_t)u.half * 64u * 128u;
+                if (pw == 0 && issuer) {   // lane l loads keys [64 l, 64 l + 64)
+                    const uint32_t dst = smem + S_RING + (uint32_t)g * KROUND + (uint32_t)lane * 64u * 128u;
 #pragma unroll
-                    for (int cc = 0; cc < RCHUNKS; ++cc)
-                        tma_tile_multicast(dst + (uint32_t)cc * KCHUNK, run_map, (g * RCHUNKS + cc) * 64, base, bar,
-                                           S_MASK);
+                    for (int cc = 0; cc < RCHUNKS; ++cc) {
+                        if constexpr (NT == 2)
+                            tma_tile_multicast(dst + (uint32_t)cc * KCHUNK, run_map, (g * RCHUNKS + cc) * 64, base, bar,
+                                               Shape<NT>::S_MASK);
+                        else
+                            tma_tile(dst + (uint32_t)cc * KCHUNK, run_map, (g * RCHUNKS + cc) * 64, base, bar);
+                    }
                 }
             } else if (issuer) {
                 const uint32_t dst = smem + S_RING + (uint32_t)g * KROUND + (uint32_t)kg * 512u;
 #pragma unroll
-                for (int cc = 0; cc < RCHUNKS; ++cc)
-                    tma_gather4_multicast(dst + (uint32_t)cc * KCHUNK, tmap, (g * RCHUNKS + cc) * 64, cur.y[0], cur.y[1],
-                                          cur.y[2], cur.y[3], bar, S_MASK);
+                for (int cc = 0; cc < RCHUNKS; ++cc) {
+                    if constexpr (NT == 2)
+                        tma_gather4_multicast(dst + (uint32_t)cc * KCHUNK, tmap, (g * RCHUNKS + cc) * 64, cur.y[0],
+                                              cur.y[1], cur.y[2], cur.y[3], bar, Shape<NT>::S_MASK);
+                    else
+                        tma_gather4(dst + (uint32_t)cc * KCHUNK, tmap, (g * RCHUNKS + cc) * 64, cur.y[0], cur.y[1],
+                                    cur.y[2], cur.y[3], bar);
+                }
             }
         }
         if (!ok) break;
@@ -355,6 +373,7 @@ __device__ void s_gather(const Params &p, Header *h, const CUtensorMap *tmap, co
 //
 // S[buf] = Q K^T round by round: 32 MMAs with Q's no-PE dims from TMEM, then
 // 4 with Q's RoPE dims from shared memory; each round is released by a commit.
+template <int NT>
 __device__ void s_mma(const Params &p, Header *h, uint32_t smem, uint32_t tmem, const Unit &u)
 {
     for (int t = 0; t < u.ntiles; ++t) {
@@ -397,7 +416,7 @@ __device__ void s_mma(const Params &p, Header *h, uint32_t smem, uint32_t tmem, 
                                sdesc_sw128(sb + 32u * (uint32_t)k, 16u, 1024u), IDESC_S, 1u);
                 }
             }
-            mma_commit_multicast(smem_u32(&h->c_empty[g]), S_MASK);   // both S CTAs may refill the slot
+            mma_commit_multicast(smem_u32(&h->c_empty[g]), Shape<NT>::S_MASK);   // every S CTA may refill the slot
         }
         if (!ok) break;
         mma_commit(smem_u32(&h->s_full[buf]));
@@ -628,18 +647,22 @@ __device__ void s_softmax(const Params &p, Header *h, uint32_t smem, uint32_t tm
 // V half tile layout: four 64-dim column blocks of 64 keys (8 KB each, key
 // rows of 128 B swizzled as above): the MN-major B operand of one N = 256
 // P V MMA.  Round R = 2 * (O tile) + value half goes to ring slot R % 4.
-// In the O CTA of row tile h, producer warp w gathers key group 8h + (w & 7)
-// (four keys of the 64), column blocks 2 (w >> 3) and 2 (w >> 3) + 1 of
-// every round, multicast to both O CTAs.  Contiguous fast path as for K
-// (decided once per unit, full O tiles only): one lane loads each column
-// block with a plain TMA tile of this CTA's 32 rows (run_map: box 64 x 32).
+// With two row tiles, in the O CTA of row tile h, producer warp w gathers
+// key group 8h + (w & 7) (four keys of the 64), column blocks 2 (w >> 3) and
+// 2 (w >> 3) + 1 of every round, multicast to both O CTAs; with one row
+// tile, warp w gathers key group w for all four column blocks.  Contiguous
+// fast path as for K (decided once per unit, full O tiles only): one lane
+// loads each column block with a plain TMA tile of this CTA's 32 rows
+// (two row tiles; run_map: box 64 x 32) or of all 64 (one; box 64 x 64).
+template <int NT>
 __device__ void o_gather(const Params &p, Header *h, const CUtensorMap *tmap, const CUtensorMap *run_map,
                          uint32_t smem, const Unit &u)
 {
+    constexpr int NB = NT == 2 ? 2 : 4;            // column blocks per warp and round
     const int pw = (int)(threadIdx.x >> 5) - PRODUCER_WARP0;
     const int lane = threadIdx.x & 31;
     const bool act = lane == 0;
-    const int kg = 8 * u.half + (pw & 7), blk0 = 2 * (pw >> 3);
+    const int kg = NT == 2 ? 8 * u.half + (pw & 7) : pw, blk0 = NT == 2 ? 2 * (pw >> 3) : 0;
     const int nt = 2 * u.ntiles;
     auto key0 = [&](int ot) { return tile_key0(u, ot >> 1) + (int64_t)(ot & 1) * KEYS_O + kg * 4; };
     RawSlots raw = load_slots(p, u, key0(0), act);
@@ -651,7 +674,7 @@ __device__ void o_gather(const Params &p, Header *h, const CUtensorMap *tmap, co
     uint32_t phase = 0;
     for (int ot = 0; ot < nt && ok; ++ot) {
         const bool run = contiguous && key0(ot) - kg * 4 + KEYS_O <= u.k1;
-        const int base = cur.y[0];                       // warp 0, lane 0: the first key of this CTA's 32
+        const int base = cur.y[0];                       // warp 0, lane 0: the first key this CTA loads
 #pragma unroll 1
         for (int hf = 0; hf < 2; ++hf) {
             const int R = 2 * ot + hf;
@@ -661,22 +684,32 @@ __device__ void o_gather(const Params &p, Header *h, const CUtensorMap *tmap, co
             }
             const uint32_t bar = smem_u32(&h->v_full[slot]);
             if (lane == 0) {
-                if (pw == 0) mbar_arrive_expect_tx(bar, VHALF);   // both O CTAs' key groups land here
+                if (pw == 0) mbar_arrive_expect_tx(bar, VHALF);   // every O CTA's key groups land here
                 else mbar_arrive(bar);
             }
             if (run) {
                 if (pw == 0 && lane == 0) {
                     const uint32_t dst = smem + O_VRING + (uint32_t)slot * VHALF + (uint32_t)u.half * 32u * 128u;
 #pragma unroll
-                    for (int blk = 0; blk < 4; ++blk)
-                        tma_tile_multicast(dst + (uint32_t)blk * VCHUNK, run_map, (4 * hf + blk) * 64, base, bar, O_MASK);
+                    for (int blk = 0; blk < 4; ++blk) {
+                        if constexpr (NT == 2)
+                            tma_tile_multicast(dst + (uint32_t)blk * VCHUNK, run_map, (4 * hf + blk) * 64, base, bar,
+                                               Shape<NT>::O_MASK);
+                        else
+                            tma_tile(dst + (uint32_t)blk * VCHUNK, run_map, (4 * hf + blk) * 64, base, bar);
+                    }
                 }
             } else if (act) {
                 const uint32_t dst = smem + O_VRING + (uint32_t)slot * VHALF + (uint32_t)kg * 512u;
 #pragma unroll
-                for (int j = 0; j < 2; ++j)
-                    tma_gather4_multicast(dst + (uint32_t)(blk0 + j) * VCHUNK, tmap, (4 * hf + blk0 + j) * 64, cur.y[0],
-                                          cur.y[1], cur.y[2], cur.y[3], bar, O_MASK);
+                for (int j = 0; j < NB; ++j) {
+                    if constexpr (NT == 2)
+                        tma_gather4_multicast(dst + (uint32_t)(blk0 + j) * VCHUNK, tmap, (4 * hf + blk0 + j) * 64,
+                                              cur.y[0], cur.y[1], cur.y[2], cur.y[3], bar, Shape<NT>::O_MASK);
+                    else
+                        tma_gather4(dst + (uint32_t)(blk0 + j) * VCHUNK, tmap, (4 * hf + blk0 + j) * 64, cur.y[0],
+                                    cur.y[1], cur.y[2], cur.y[3], bar);
+                }
             }
             if (++slot == NVH) { slot = 0; phase ^= 1u; }
         }
@@ -693,6 +726,7 @@ __device__ void o_gather(const Params &p, Header *h, const CUtensorMap *tmap, co
 //
 // O += P V per 64-key O tile: two halves of the value dims, N = 256 each.
 // P slot [g][par] of O tile ot: g = ot & 1 (softmax group), par = (ot >> 1) & 1.
+template <int NT>
 __device__ void o_mma(const Params &p, Header *h, uint32_t smem, uint32_t tmem, const Unit &u)
 {
     const int nt = 2 * u.ntiles;
@@ -727,7 +761,7 @@ __device__ void o_mma(const Params &p, Header *h, uint32_t smem, uint32_t tmem, 
             for (int k = 0; k < KEYS_O / 16; ++k)
                 mma_ss(tmem + 256u * (uint32_t)hf, sdesc_sw128(pb + 32u * (uint32_t)k, 16u, 1024u),
                        sdesc_sw128(vb + (uint32_t)k * 16u * 128u, VCHUNK, 1024u), IDESC_PV, (ot | k) ? 1u : 0u);
-            mma_commit_multicast(smem_u32(&h->v_empty[slot]), O_MASK);   // both O CTAs may refill the slot
+            mma_commit_multicast(smem_u32(&h->v_empty[slot]), Shape<NT>::O_MASK);   // every O CTA may refill the slot
             if (++slot == NVH) { slot = 0; phase ^= 1u; }
         }
         if (!ok) break;
@@ -792,7 +826,9 @@ __device__ void o_rows(const Params &p, Header *h, uint32_t smem, uint32_t tmem,
     }
 }
 
-__global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(THREADS, 1)
+// Launched with clusters of 2 * NT CTAs (a launch attribute).
+template <int NT>
+__global__ void __launch_bounds__(THREADS, 1)
     tc_split_kernel(Params p, const __grid_constant__ CUtensorMap pool_map,
                     const __grid_constant__ CUtensorMap run_map_k, const __grid_constant__ CUtensorMap run_map_v)
 {
@@ -804,12 +840,13 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(THREADS, 1)
     const uint32_t role = rank & 1u;        // 0: S, 1: O
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
-    // Segment decode.  All four CTAs of the cluster compute the same unit, so
-    // they leave together when it is empty.  Grid: x = 4 * pair of row tiles
-    // + rank, y = split, z = request; pairs vary fastest, so clusters that
-    // read the same key chunk run together and share it through L2.  The
-    // second row tile of a pair may be past the request's rows: its CTAs
-    // still take part (their gathers feed the first row tile) on zero rows.
+    // Segment decode.  All CTAs of the cluster compute the same unit, so
+    // they leave together when it is empty.  Grid: x = 2 NT * (group of NT
+    // row tiles) + rank, y = split, z = request; row groups vary fastest, so
+    // clusters that read the same key chunk run together and share it
+    // through L2.  With NT = 2 the second row tile may be past the request's
+    // rows: its CTAs still take part (their gathers feed the first row tile)
+    // on zero rows.
     Unit u;
     u.split = (int)blockIdx.y;
     u.b = (int)blockIdx.z;
@@ -823,9 +860,9 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(THREADS, 1)
         if (T < 0 || u.L < 0) return;
     }
     u.rows_b = (T < p.max_q_per_req ? T : p.max_q_per_req) * p.num_heads;
-    const int64_t pair = blockIdx.x >> 2;
-    if (2 * pair * ROWS >= u.rows_b) return;
-    u.r0 = (2 * pair + u.half) * ROWS;
+    const int64_t first_row = (int64_t)(blockIdx.x / (2 * NT)) * (NT * ROWS);   // the cluster's first row
+    if (first_row >= u.rows_b) return;
+    u.r0 = first_row + (int64_t)u.half * ROWS;
     u.N = u.L + T;
     const int64_t chunk = split_chunk(u.N, p.num_splits);
     u.k0 = (int64_t)u.split * chunk;
@@ -836,11 +873,11 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(THREADS, 1)
     if (tid == 0) {
         for (int s = 0; s < NKR; ++s) {
             mbar_init(smem_u32(&h->c_full[s]), PRODUCER_WARPS);
-            mbar_init(smem_u32(&h->c_empty[s]), 2);
+            mbar_init(smem_u32(&h->c_empty[s]), NT);
         }
         for (int s = 0; s < NVH; ++s) {
             mbar_init(smem_u32(&h->v_full[s]), PRODUCER_WARPS);
-            mbar_init(smem_u32(&h->v_empty[s]), 2);
+            mbar_init(smem_u32(&h->v_empty[s]), NT);
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(smem_u32(&h->s_full[i]), 2);
@@ -865,7 +902,7 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(THREADS, 1)
     }
     if (warp == PRODUCER_WARP0 && lane == 0) {
         prefetch_tensormap(&pool_map);
-        prefetch_tensormap(role == 0 ? &run_map_k : &run_map_v);
+        prefetch_tensormap(role == 0 || NT == 1 ? &run_map_k : &run_map_v);
     }
     if (warp == MMA_WARP) {
         tmem_alloc(smem_u32(&h->tmem_base), TMEM_COLS);
@@ -889,15 +926,15 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(THREADS, 1)
     } else {
         regs_dec<REGS_NARROW>();
         if (warp >= PRODUCER_WARP0 && warp < MMA_WARP) {
-            if (role == 0) s_gather(p, h, &pool_map, &run_map_k, smem, u);
-            else o_gather(p, h, &pool_map, &run_map_v, smem, u);
+            if (role == 0) s_gather<NT>(p, h, &pool_map, &run_map_k, smem, u);
+            else o_gather<NT>(p, h, &pool_map, NT == 2 ? &run_map_v : &run_map_k, smem, u);
         } else if (warp == MMA_WARP) {
             if (role == 0) {
                 named_barrier_sync(1, SOFTMAX_THREADS + 32);
                 tc_fence_after_sync();
-                if (lane == 0) s_mma(p, h, smem, tmem, u);
+                if (lane == 0) s_mma<NT>(p, h, smem, tmem, u);
             } else if (lane == 0) {
-                o_mma(p, h, smem, tmem, u);
+                o_mma<NT>(p, h, smem, tmem, u);
             }
         }
         __syncwarp();
@@ -947,24 +984,55 @@ cudaError_t tc_init()
     if (g_encode == nullptr) return cudaErrorNotSupported;
     // setmaxnreg.inc waits for registers the CTA does not have if the
     // launch allocation is smaller than the split assumes: refuse to run.
-    cudaFuncAttributes fa;
-    cudaError_t e = cudaFuncGetAttributes(&fa, tc_split_kernel);
-    if (e != cudaSuccess) return e;
-    if (fa.numRegs < LAUNCH_REGS || fa.maxThreadsPerBlock < THREADS) return cudaErrorNotSupported;
-    return cudaFuncSetAttribute(tc_split_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_ALLOC);
+    for (const void *fn : {reinterpret_cast<const void *>(tc_split_kernel<1>),
+                           reinterpret_cast<const void *>(tc_split_kernel<2>)}) {
+        cudaFuncAttributes fa;
+        cudaError_t e = cudaFuncGetAttributes(&fa, fn);
+        if (e != cudaSuccess) return e;
+        if (fa.numRegs < LAUNCH_REGS || fa.maxThreadsPerBlock < THREADS) return cudaErrorNotSupported;
+        e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_ALLOC);
+        if (e != cudaSuccess) return e;
+    }
+    return cudaSuccess;
 }
 
 bool tc_supported(const Params &p) { return p.pool_size < ((int64_t)1 << 31); }
+
+namespace {
+
+template <int NT>
+cudaError_t launch_shape(const Params &p, const CUtensorMap &map, const CUtensorMap &run_k, const CUtensorMap &run_v,
+                         cudaStream_t stream)
+{
+    const int groups = (int)((p.max_q_per_req * (int64_t)p.num_heads + NT * ROWS - 1) / (NT * ROWS));
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(2u * NT * (unsigned)groups, (unsigned)p.num_splits, (unsigned)p.batch);
+    cfg.blockDim = dim3(THREADS, 1, 1);
+    cfg.dynamicSmemBytes = SMEM_ALLOC;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2 * NT;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, tc_split_kernel<NT>, p, map, run_k, run_v);
+}
+
+}  // namespace
+
+// One row tile per cluster when every request's rows fit one (T * H <= 128),
+// else two.
+int tc_row_tiles(const Params &p) { return p.max_q_per_req * (int64_t)p.num_heads <= ROWS ? 1 : 2; }
 
 cudaError_t launch_tc_split(const Params &p, cudaStream_t stream)
 {
     CUtensorMap map, run_k, run_v;
     if (!encode_pool_map(p, &map) || !encode_pool_map(p, &run_k, 64) || !encode_pool_map(p, &run_v, 32))
         return cudaErrorInvalidValue;
-    const int pairs = (int)((p.max_q_per_req * (int64_t)p.num_heads + 2 * ROWS - 1) / (2 * ROWS));
-    dim3 grid(4u * (unsigned)pairs, (unsigned)p.num_splits, (unsigned)p.batch);
-    tc_split_kernel<<<grid, THREADS, SMEM_ALLOC, stream>>>(p, map, run_k, run_v);
-    return cudaGetLastError();
+    return tc_row_tiles(p) == 1 ? launch_shape<1>(p, map, run_k, run_v, stream)
+                                : launch_shape<2>(p, map, run_k, run_v, stream);
 }
 
 }  // namespace va

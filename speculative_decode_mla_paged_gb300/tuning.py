@@ -14,6 +14,8 @@ from typing import Sequence
 NUM_SMS = 152                  # GB300: 2 dies x 76 SMs
 TC_CLUSTERS = 36               # 4-CTA clusters of the tensor-core kernel resident at once on a GB300
                                # (a cluster stays inside one GPC: 144 of the 152 SMs)
+TC_CLUSTERS_ONE_TILE = 76      # 2-CTA clusters resident at once (the shape used when T * H <= 128)
+TC_TILE_ROWS = 128             # rows per row tile of the tensor-core kernel
 KEY_ALIGN = 128                # must match the library's split chunk rule
 MIN_CHUNK = 256
 CANDIDATES = tuple(range(1, 65)) + (72, 80, 96, 108, 128, 144, 160, 192, 256)
@@ -34,17 +36,20 @@ def simulate(prefix_lens: Sequence[int], draft_lens: Sequence[int], num_heads: i
     """Estimated time of one call in units of one key tile of a unit.
 
     Units are dispatched in grid order (row group fastest, then split, then
-    request) onto the concurrent slots (36 four-CTA clusters of 256 rows for
-    the tensor-core kernel, 128-key tiles; 304 CTAs of 16 rows for the
-    CUDA-core one, 32-key tiles); each costs its key tiles plus a fixed
-    start-up (query load, pipeline fill, partial write).  The combine's
-    workspace traffic is added on top.
+    request) onto the concurrent slots (tensor-core kernel: 36 four-CTA
+    clusters of 256 rows, or 76 two-CTA clusters of 128 rows when every
+    request has T * H <= 128, 128-key tiles; CUDA-core kernel: 304 CTAs of 16
+    rows, 32-key tiles); each costs its key tiles plus a fixed start-up (query
+    load, pipeline fill, partial write).  The combine's workspace traffic is
+    added on top.
     """
+    max_q = max(draft_lens) if len(draft_lens) else 0
     if kernel == "simt":
         rows, slots, overhead, tile_keys, tile_cost, tile_s = 16, 2 * NUM_SMS, 2.0, 32, 1.0, 0.5e-6
+    elif max_q * num_heads <= TC_TILE_ROWS:
+        rows, slots, overhead, tile_keys, tile_cost, tile_s = TC_TILE_ROWS, TC_CLUSTERS_ONE_TILE, 4.0, 128, 1.0, 2.5e-6
     else:
-        rows, slots, overhead, tile_keys, tile_cost, tile_s = 256, TC_CLUSTERS, 4.0, 128, 1.0, 2.5e-6
-    max_q = max(draft_lens) if len(draft_lens) else 0
+        rows, slots, overhead, tile_keys, tile_cost, tile_s = 2 * TC_TILE_ROWS, TC_CLUSTERS, 4.0, 128, 1.0, 2.5e-6
     max_tiles = math.ceil(max_q * num_heads / rows)
     free = [0.0] * slots
     heapq.heapify(free)

@@ -61,14 +61,16 @@ def test_extra_workloads(name, impl):
 
 
 @pytest.mark.parametrize("slots", ["runs:64", "runs:37", "runs:200", "contiguous"])
-def test_contiguous_runs_every_row(slots):
-    """Pools cut into runs of consecutive slots: some 64-key (K) and 32-key
-    (V) shares of a tile are contiguous and take plain TMA tiles, the others
-    gathers; every output row against the oracle."""
-    inp = W.make_inputs([3000, 1500, 700], [32, 16, 8], 8, 65536, seed=41, slots=slots)
+@pytest.mark.parametrize("drafts", [(32, 16, 8), (16, 8, 4)], ids=["two_row_tiles", "one_row_tile"])
+def test_contiguous_runs_every_row(slots, drafts):
+    """Pools cut into runs of consecutive slots: units whose keys are all
+    consecutive take plain TMA tiles, the others gathers; with T * H up to
+    256 (4-CTA clusters) and up to 128 (2-CTA clusters); every output row
+    against the oracle."""
+    inp = W.make_inputs([3000, 1500, 700], list(drafts), 8, 65536, seed=41, slots=slots)
     out, status = run(inp, impl="tc", num_splits=3)
     assert status == 0
-    assert_parity(as_rows(out), oracle_rows(inp), f"tc/{slots}")
+    assert_parity(as_rows(out), oracle_rows(inp), f"tc/{slots}/{drafts}")
 
 
 @pytest.mark.parametrize("impl", IMPLS)
