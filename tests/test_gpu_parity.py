@@ -256,14 +256,17 @@ def test_mask_decode_bit_exact(impl):
 
 # ---------------------------------------------------------------- CUDA graph capture / replay
 
+@pytest.mark.parametrize("max_q", [16, 32], ids=["one_row_tile", "two_row_tiles"])
 @pytest.mark.parametrize("impl", IMPLS)
-def test_graph_capture_and_replay_with_new_contents(impl):
+def test_graph_capture_and_replay_with_new_contents(impl, max_q):
     """Capture one call, then rewrite the *contents* of the static buffers
     (new trees, new slots, new prefix lengths, new q) and replay: each replay
     must match the oracle on the new inputs ("The Capture-Safe Kernel",
-    Decision 6: no replay hook, the kernel reads the static buffers)."""
-    B, max_q, H, splits, pool_size = 3, 16, 8, 8, 8192
-    cap_kv, cap_bits = 3 * 1500, 3 * 16 * (1500 + 16)
+    Decision 6: no replay hook, the kernel reads the static buffers).  With
+    H = 8, max_q 16 launches the tensor-core kernel's 2-CTA cluster shape and
+    max_q 32 its 4-CTA shape."""
+    B, H, splits, pool_size = 3, 8, 8, 8192
+    cap_kv, cap_bits = 3 * 1500, 3 * max_q * (1500 + max_q)
     pool = W.make_inputs([1], [1], H, pool_size=pool_size, seed=30).kv_pool.cuda()
     st = {
         "q": torch.zeros(B * max_q, H, 576, dtype=torch.bfloat16, device="cuda"),
@@ -288,7 +291,7 @@ def test_graph_capture_and_replay_with_new_contents(impl):
         runner(st["q"], pool, st["qo_indptr"], st["kv_indptr"], st["kv_indices"], st["out_cache_loc"],
                st["custom_mask"], st["mask_indptr"], W.SM_SCALE, out)
 
-    first = W.make_inputs([1000, 10, 400], [16, 3, 9], H, pool_size=pool_size, seed=31)
+    first = W.make_inputs([1000, 10, 400], [max_q, 3, 9], H, pool_size=pool_size, seed=31)
     first.kv_pool = pool.cpu()
     fill(first)
     call()                                   # warm-up outside capture
@@ -299,7 +302,7 @@ def test_graph_capture_and_replay_with_new_contents(impl):
         with torch.cuda.graph(g, stream=s):
             call()
     torch.cuda.synchronize()
-    for seed, prefix, drafts in [(32, [1500, 700, 1], [5, 16, 2]), (33, [3, 1400, 1499], [16, 1, 16]),
+    for seed, prefix, drafts in [(32, [1500, 700, 1], [5, max_q, 2]), (33, [3, 1400, 1499], [max_q, 1, 16]),
                                  (34, [0, 0, 1200], [2, 2, 2])]:
         inp = W.make_inputs(prefix, drafts, H, pool_size=pool_size, seed=seed)
         inp.kv_pool = pool.cpu()
