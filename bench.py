@@ -7,7 +7,9 @@ fraction of the roofline max(FLOPs / bf16 peak, bytes / HBM bandwidth).
 One step = one full call of the hot path (status clear, split kernel, split
 combine) on one batch of the headline workload, inputs resident in HBM.  L2
 is flushed (a 256 MiB write) before every timed call; each call is timed with
-CUDA events on its own stream.  Prints ONE JSON line.
+CUDA events on its own stream.  The line also carries the same call warm (no
+flush, back to back), as cold replays of a CUDA graph holding one call, and
+end to end from pinned host buffers.  Prints ONE JSON line.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
                   [--config ragged|long|mid|short|tiny] [--kernel tc|simt]
@@ -278,6 +280,48 @@ def measure(inp, d, runner, steps, warmup, flush, torch):
     return call_ms, split_ms, comb_ms
 
 
+def measure_warm(inp, d, runner, steps, torch):
+    """Device time per call of `steps` back-to-back calls with no L2 flush
+    (inputs partly L2-resident from the previous call)."""
+    def call():
+        runner(d["q"], d["kv_pool"], d["qo_indptr"], d["kv_indptr"], d["kv_indices"], d["out_cache_loc"],
+               d["custom_mask"], d["mask_indptr"], inp.sm_scale, d["out"])
+
+    call()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(steps):
+        call()
+    e1.record()
+    e1.synchronize()
+    return e0.elapsed_time(e1) / steps
+
+
+def measure_graph(inp, d, runner, steps, warmup, flush, torch):
+    """Device time per replay of one call captured in a CUDA graph, each
+    replay after an L2 flush (the flush is outside the timed events)."""
+    s = torch.cuda.Stream()
+    g = torch.cuda.CUDAGraph()
+    torch.cuda.synchronize()
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(g, stream=s):
+            runner(d["q"], d["kv_pool"], d["qo_indptr"], d["kv_indptr"], d["kv_indices"], d["out_cache_loc"],
+                   d["custom_mask"], d["mask_indptr"], inp.sm_scale, d["out"])
+    torch.cuda.synchronize()
+    ts = []
+    for k in range(warmup + steps):
+        flush.zero_()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        g.replay()
+        e1.record()
+        e1.synchronize()
+        if k >= warmup:
+            ts.append(e0.elapsed_time(e1))
+    return statistics.mean(ts)
+
+
 def device_tensors(inp, torch, dev):
     from speculative_decode_mla_paged_gb300 import api  # noqa: F401
     d = {k: torch.from_numpy(np.ascontiguousarray(getattr(inp, k))).to(dev)
@@ -353,6 +397,12 @@ def run_ours(args):
             e2e_ms.append(e0.elapsed_time(e1))
     e2e_us = per_call_us(max_over_ranks(sum(e2e_ms), world, dev), args.steps, world)
 
+    # ---- the same call warm (no flush) and as cold CUDA-graph replays
+    warm_us = measure_warm(inp, d, runner, args.steps, torch) * 1e3
+    graph_us = measure_graph(inp, d, runner, args.steps, args.warmup, flush, torch) * 1e3
+    if runner.status() != 0:
+        raise RuntimeError(f"device status word {runner.status():#x}")
+
     # ---- roofline of the dominant kernel (the split kernel)
     flops = inp.algorithmic_flops()
     nbytes = inp.algorithmic_bytes()
@@ -388,6 +438,9 @@ def run_ours(args):
                 "d2h_bytes_per_step": int(d2h_bytes)},
         "gpu_launches": 2 * args.steps,
         "clocks": clocks,
+        "warm": {"value": warm_us, "unit": UNIT, "l2": "not flushed (back-to-back calls)"},
+        "graph": {"value": graph_us, "unit": UNIT, "l2": "flushed before every replay",
+                  "what": "one call captured in a CUDA graph, device time per replay"},
     }
 
     # ---- the five workloads and the two extra ones (chain verify, decode),
@@ -419,10 +472,17 @@ def run_ours(args):
         oracle.build()
         inp.q, inp.kv_pool = inp.q.cpu(), inp.kv_pool.cpu()
         us, sample = time_oracle(inp, args.cpu_seconds)
-        line["cpu_baseline"] = {"value": us, "unit": UNIT, "cores": oracle.num_threads(), "kind": "oracle",
+        cores = oracle.num_threads()
+        line["cpu_baseline"] = {"value": us, "unit": UNIT, "cores": cores, "kind": "oracle",
                                 "sample": f"{sample['rows']} of {sample['of_rows']} output rows "
                                           f"({sample['seconds']} s), scaled to a full call by visible "
                                           "(row, key) pairs"}
+        oracle.set_num_threads(1)
+        us1, sample1 = time_oracle(inp, min(3.0, args.cpu_seconds / 4), seed=1)
+        oracle.set_num_threads(cores)
+        line["cpu_baseline"]["single_core"] = {
+            "value": us1, "unit": UNIT, "cores": 1,
+            "sample": f"{sample1['rows']} output rows ({sample1['seconds']} s), scaled the same way"}
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:

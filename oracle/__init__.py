@@ -54,12 +54,19 @@ def _load():
                                                p, i64, ctypes.c_int, p, p]
             lib.oracle_verify_attn.restype = ctypes.c_int
             lib.oracle_num_threads.restype = ctypes.c_int
+            if hasattr(lib, "oracle_set_num_threads"):
+                lib.oracle_set_num_threads.argtypes = [ctypes.c_int]
             _lib = lib
     return _lib
 
 
 def num_threads() -> int:
     return int(_load().oracle_num_threads())
+
+
+def set_num_threads(n: int) -> None:
+    """Thread count for later calls (for timing; the results do not depend on it)."""
+    _load().oracle_set_num_threads(int(n))
 
 
 def _bits16(x) -> np.ndarray:

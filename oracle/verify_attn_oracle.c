@@ -283,6 +283,17 @@ int oracle_verify_attn(const uint16_t *q, int64_t q_stride_tok, int64_t q_stride
     return err;
 }
 
+/* Threads for later calls (timing only; results do not depend on it). */
+void oracle_set_num_threads(int n)
+{
+#ifdef _OPENMP
+    extern void omp_set_num_threads(int);
+    if (n > 0) omp_set_num_threads(n);
+#else
+    (void)n;
+#endif
+}
+
 /* Number of OpenMP threads the oracle runs with (1 when built without OpenMP). */
 int oracle_num_threads(void)
 {
