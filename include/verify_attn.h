@@ -179,7 +179,10 @@ VERIFY_ATTN_API int verify_attn_run_simt(const void *q, int64_t q_stride_tok, in
  * at the start of the call, just before the split kernel (after the status
  * word is cleared), between the split kernel and the combine, and after the
  * combine.  Lets a caller time each of the two kernels on the stream they
- * run on.  Same return codes; an unknown impl gives VA_ERR_DIMS.
+ * run on.  Under stream capture the marks are recorded as external event
+ * records (cudaEventRecordExternal), so they become event-record nodes of the
+ * graph and time every replay.  Same return codes; an unknown impl gives
+ * VA_ERR_DIMS.
  */
 VERIFY_ATTN_API int verify_attn_run_profiled(int impl, void *const *events,
                                              const void *q, int64_t q_stride_tok, int64_t q_stride_head,

@@ -35,6 +35,7 @@ struct Params {
     int64_t out_stride_tok, out_stride_head;
     int batch, max_q_per_req, num_heads, num_splits;
     int64_t rows_cap;      // batch * max_q_per_req * num_heads
+    int64_t rows_lo, rows_hi;   // tensor-core split: only requests with rows_lo < T_b * H <= rows_hi
     unsigned *status;      // workspace byte 0
     float *part_o;         // [num_splits][rows_cap][512]
     float *part_lse;       // [num_splits][rows_cap]

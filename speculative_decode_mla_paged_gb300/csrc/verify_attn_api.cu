@@ -90,6 +90,8 @@ int prepare(Params &p, const void *q, int64_t q_st, int64_t q_sh, const void *kv
     p.num_heads = heads;
     p.num_splits = splits;
     p.rows_cap = (int64_t)batch * max_q * heads;
+    p.rows_lo = -1;
+    p.rows_hi = INT64_MAX;
     unsigned char *ws = static_cast<unsigned char *>(workspace);
     p.status = reinterpret_cast<unsigned *>(ws);
     p.part_o = reinterpret_cast<float *>(ws + WS_HEADER);
@@ -124,8 +126,14 @@ int run(Impl impl, const void *q, int64_t q_st, int64_t q_sh, const void *kv_poo
     rc = ensure_init();
     if (rc != VA_OK) return rc;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    // Under stream capture the marks are external records (event-record nodes
+    // of the graph, so every replay records them); otherwise plain records.
+    cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+    if (events != nullptr && cudaStreamIsCapturing(s, &cap) != cudaSuccess) return VA_ERR_LAUNCH;
+    const unsigned rec_flags = cap == cudaStreamCaptureStatusActive ? cudaEventRecordExternal : cudaEventRecordDefault;
     auto mark = [&](int k) {
-        return events == nullptr || events[k] == nullptr || cudaEventRecord(events[k], s) == cudaSuccess;
+        return events == nullptr || events[k] == nullptr ||
+               cudaEventRecordWithFlags(events[k], s, rec_flags) == cudaSuccess;
     };
     if (!mark(0)) return VA_ERR_LAUNCH;
     if (cudaMemsetAsync(p.status, 0, sizeof(unsigned), s) != cudaSuccess) return VA_ERR_LAUNCH;

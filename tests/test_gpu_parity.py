@@ -311,3 +311,37 @@ def test_graph_capture_and_replay_with_new_contents(impl, max_q):
         torch.cuda.synchronize()
         got = as_rows(out)[: inp.total_q * H]
         assert_parity(got, oracle_rows(inp), f"replay seed {seed}/{impl}")
+
+
+def test_profiled_call_times_every_graph_replay():
+    """The library's phase events time a direct call and, recorded inside a
+    captured graph (external event records), each replay: start <= split
+    start <= split end <= combine end, all readable, and the output still
+    matches the oracle."""
+    inp = W.make_inputs([1200, 300], [24, 8], 8, 8192, seed=61)
+    d = device_inputs(inp)
+    runner = api.VerifyAttention(inp.batch, inp.max_q_per_req, inp.num_heads, 4)
+    out = torch.zeros(inp.total_q, inp.num_heads, 512, dtype=torch.bfloat16, device="cuda")
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+
+    def call():
+        runner(d["q"], d["kv_pool"], d["qo_indptr"], d["kv_indptr"], d["kv_indices"], d["out_cache_loc"],
+               d["custom_mask"], d["mask_indptr"], inp.sm_scale, out, events=ev)
+
+    call()                                   # a direct profiled call first
+    torch.cuda.synchronize()
+    t = [ev[0].elapsed_time(e) for e in ev]
+    assert t[0] == 0 and 0 <= t[1] <= t[2] <= t[3] < 1000.0, t
+    g = torch.cuda.CUDAGraph()
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(g, stream=s):
+            call()
+    for _ in range(3):
+        out.zero_()
+        g.replay()
+        torch.cuda.synchronize()
+        t = [ev[0].elapsed_time(e) for e in ev]
+        assert t[0] == 0 and 0 <= t[1] <= t[2] <= t[3] < 1000.0, t
+        assert_parity(as_rows(out), oracle_rows(inp), "profiled replay")
+    assert runner.status() == 0
