@@ -85,7 +85,8 @@ def kernel_hash(kernel):
 
 
 def profiled_traffic(kernel, cfg_name):
-    """DRAM bytes per launch from a committed ncu summary for this exact kernel source."""
+    """DRAM bytes of the split phase of one call (all its split launches) from
+    a committed ncu summary for this exact kernel source."""
     path = os.path.join(ROOT, "profiles", "dram_traffic.md")
     if not os.path.exists(path):
         return None
@@ -439,7 +440,8 @@ def run_ours(args):
     roof["frac"] = roof["achieved"] / roof["peak"]
     roof["traffic"] = profiled_traffic(args.kernel, args.config)
     roof["peak_source"] = f"{peak_src} (burst; kernel timed alone)"
-    roof["kernel"] = f"{args.kernel} split kernel"
+    roof["kernel"] = (f"{args.kernel} split phase (the split launches of one call, concurrent when both "
+                      "tensor-core cluster shapes run; traffic summed over them)")
     roof["algorithmic_flops"] = flops
     roof["algorithmic_bytes"] = nbytes
 

@@ -28,11 +28,18 @@
  *
  * Contract of every entry point that takes a stream:
  *   - all tensor pointers are DEVICE pointers owned by the caller;
- *   - the library keeps no per-call state, allocates nothing, never
- *     synchronises, and launches only on `stream` (0 = legacy default
- *     stream), so a call can be captured into a CUDA graph and replayed
- *     after the caller rewrites the *contents* of its buffers (Decision 6:
- *     no replay-metadata hook needed);
+ *   - the library keeps no per-call state, allocates no device memory and
+ *     never synchronises, so a call can be captured into a CUDA graph and
+ *     replayed after the caller rewrites the *contents* of its buffers
+ *     (Decision 6: no replay-metadata hook needed).  Work is ordered on
+ *     `stream` (0 = legacy default stream): when a call may hold requests
+ *     of both tensor-core cluster shapes (max_q_per_req * num_heads > 128),
+ *     the small requests' launch runs on a library-owned second stream,
+ *     forked from `stream` by an event before it and joined back by an
+ *     event before the combine, which stream capture records as a fork and
+ *     a join of the graph.  Per device the library holds that stream, its
+ *     two events (created by verify_attn_init) and the tensor-map
+ *     descriptors of the last pool it saw (host memory);
  *   - host-side argument errors are reported by a negative VA_ERR_* return
  *     and nothing is launched;
  *   - device-side data errors never trap: a slot id outside [0, pool_size)
@@ -42,7 +49,9 @@
  *     reads it after its own synchronisation.
  *
  * Thread safety: calls may be made from several host threads; concurrent
- * calls must use distinct workspaces.
+ * calls must use distinct workspaces.  Mixed-shape calls on one device share
+ * the library's second stream (a lock keeps each call's fork, launch and
+ * join together), so their small-request launches run one after another.
  */
 #ifndef VERIFY_ATTN_H
 #define VERIFY_ATTN_H
