@@ -79,9 +79,35 @@ def default_splits(cfg_name, inp, kernel):
     return tuning.plan_num_splits(inp.prefix_lens, inp.draft_lens, inp.num_heads, kernel)
 
 
+def code_text(src: str) -> str:
+    """C++/CUDA source without comments and whitespace: what the compiler sees."""
+    out, i, n = [], 0, len(src)
+    while i < n:
+        if src.startswith("//", i):
+            i = src.find("\n", i)
+            i = n if i < 0 else i
+        elif src.startswith("/*", i):
+            j = src.find("*/", i + 2)
+            i = n if j < 0 else j + 2
+        elif src[i] == '"':                      # string literal, kept as written
+            j = i + 1
+            while j < n and src[j] != '"':
+                j += 2 if src[j] == "\\" else 1
+            out.append(src[i:j + 1])
+            i = j + 1
+        else:
+            if not src[i].isspace():
+                out.append(src[i])
+            i += 1
+    return "".join(out)
+
+
 def kernel_hash(kernel):
-    with open(os.path.join(ROOT, KERNEL_SOURCES[kernel]), "rb") as f:
-        return hashlib.sha1(f.read()).hexdigest()[:12]
+    """First 12 hex digits of the SHA-1 of the kernel source's code text
+    (comments and whitespace removed, so an edit to a comment keeps a
+    capture valid)."""
+    with open(os.path.join(ROOT, KERNEL_SOURCES[kernel]), encoding="utf-8") as f:
+        return hashlib.sha1(code_text(f.read()).encode()).hexdigest()[:12]
 
 
 def profiled_traffic(kernel, cfg_name):

@@ -9,7 +9,9 @@
 // tensor cores.
 //
 // A 4-CTA cluster per unit: ranks 2h and 2h + 1 serve row tile h of the
-// pair.  A 128 x 512 fp32 output accumulator is the whole of an SM's TMEM
+// pair (a request with at most 128 rows runs on a 2-CTA cluster of one row
+// tile instead: see the cluster shapes below and launch_tc_split).  A
+// 128 x 512 fp32 output accumulator is the whole of an SM's TMEM
 // (128 lanes x 512 columns), so one SM cannot hold Q, the scores S and O for
 // 128 rows; the two CTAs of a row tile split the work by role:
 //
@@ -31,9 +33,10 @@
 // Per 128-key tile the S CTA issues 36 MMAs (M128 N128 K16) and the O CTA 16
 // (M128 N256 K16): 576 and 512 MACs per (row, key), balanced.
 //
-// Gathers are the throughput limit of this design (a TMA gather4 moves
-// 512 B, and one warp issues them one at a time, lane after lane).  The two
-// S CTAs need the same K tiles and the two O CTAs the same V tiles, so each
+// The gathers set the pace (a TMA gather4 moves 512 B, and one warp issues
+// them one at a time, lane after lane; a ring slot comes back only after its
+// refill's issue and flight and the MMAs that read it).  The two S CTAs
+// need the same K tiles and the two O CTAs the same V tiles, so each
 // gathers half of every tile and multicasts it into both; a ring slot is
 // reused once both consumers' MMAs have released it (tensor-core commits
 // multicast to both).  Each CTA runs 16 producer warps that share every
