@@ -270,7 +270,7 @@ def run_reference(args):
         "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": value / 1e3,
         "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-        "data": "synthetic", "config": {"workload": W.CONFIGS[args.config].description,
+        "data": "synthetic", "config": {"workload": f"{args.config}: {W.CONFIGS[args.config].description}",
                                         "name": args.config},
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
                          "sample": f"per step {samples[0]['rows']} of {samples[0]['of_rows']} output rows "
