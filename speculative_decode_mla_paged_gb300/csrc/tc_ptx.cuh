@@ -1,6 +1,7 @@
-// Thin inline-PTX wrappers for sm_103a: mbarriers, cluster addressing,
-// cp.async and TMA gathers, tcgen05 (TMEM allocation, MMA, commit, TMEM loads and
-// stores) and shared-memory matrix descriptors.  Written from the PTX ISA
+// Thin inline-PTX wrappers for sm_103a: mbarriers, cluster addressing and
+// barriers, TMA tile / gather4 loads and bulk copies, tcgen05 (TMEM
+// allocation, MMA, commit, TMEM loads and stores) and shared-memory matrix
+// descriptors.  Written from the PTX ISA
 // descriptions of these instructions.
 #pragma once
 
@@ -136,49 +137,11 @@ __device__ __forceinline__ void fence_proxy_async_smem()
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
-// Orders this thread's generic-proxy accesses to (any CTA's) shared memory
-// before later async-proxy accesses.
-__device__ __forceinline__ void fence_proxy_async_cluster()
-{
-    asm volatile("fence.proxy.async.shared::cluster;" ::: "memory");
-}
-
 // ------------------------------------------------------------------ distributed shared memory stores
-
-__device__ __forceinline__ void st_cluster_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d)
-{
-    asm volatile("st.shared::cluster.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d)
-                 : "memory");
-}
 
 __device__ __forceinline__ void st_cluster_f32(uint32_t addr, float v)
 {
     asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
-}
-
-__device__ __forceinline__ void st_cluster_u8(uint32_t addr, uint32_t v)
-{
-    asm volatile("st.shared::cluster.u8 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
-}
-
-// ------------------------------------------------------------------ cp.async gathers
-
-// 16-byte global -> shared copy; src_bytes = 0 writes zeros and reads nothing.
-__device__ __forceinline__ void cp_async16(uint32_t dst, const void *src, uint32_t src_bytes)
-{
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes) : "memory");
-}
-
-// The barrier receives one arrival once every cp.async this thread issued
-// before has landed (its expected count must include this arrival).
-__device__ __forceinline__ void cp_async_arrive_noinc(uint32_t bar)
-{
-    asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
-}
-
-__device__ __forceinline__ void cp_async_wait_all()
-{
-    asm volatile("cp.async.wait_all;" ::: "memory");
 }
 
 // ------------------------------------------------------------------ TMA
