@@ -345,3 +345,41 @@ def test_profiled_call_times_every_graph_replay():
         assert t[0] == 0 and 0 <= t[1] <= t[2] <= t[3] < 1000.0, t
         assert_parity(as_rows(out), oracle_rows(inp), "profiled replay")
     assert runner.status() == 0
+
+
+def test_concurrent_mixed_calls_from_two_threads():
+    """Two host threads, each with its own workspace and stream, issue mixed
+    calls (both cluster shapes, so both go through the library's shared second
+    stream and its lock) at the same time; every output matches the oracle."""
+    import threading
+
+    cases = [W.make_inputs([900, 200, 40], [24, 8, 16], 8, 8192, seed=81),
+             W.make_inputs([300, 1200], [8, 32], 8, 8192, seed=82)]
+    refs = [oracle_rows(c) for c in cases]
+    devs = [device_inputs(c) for c in cases]
+    torch.cuda.synchronize()                  # inputs copied before other streams read them
+    errors = []
+
+    def worker(k):
+        try:
+            c, d = cases[k], devs[k]
+            runner = api.VerifyAttention(c.batch, c.max_q_per_req, c.num_heads, 4)
+            s = torch.cuda.Stream()
+            out = torch.zeros(c.total_q, c.num_heads, 512, dtype=torch.bfloat16, device="cuda")
+            for _ in range(20):
+                with torch.cuda.stream(s):
+                    out.zero_()
+                    runner(d["q"], d["kv_pool"], d["qo_indptr"], d["kv_indptr"], d["kv_indices"],
+                           d["out_cache_loc"], d["custom_mask"], d["mask_indptr"], c.sm_scale, out)
+                s.synchronize()
+                assert runner.status() == 0
+                assert_parity(as_rows(out), refs[k], f"thread {k}")
+        except Exception as e:          # reported in the main thread
+            errors.append(e)
+
+    threads = [threading.Thread(target=worker, args=(k,)) for k in range(2)]
+    for t in threads:
+        t.start()
+    for t in threads:
+        t.join()
+    assert not errors, errors
