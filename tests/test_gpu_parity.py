@@ -383,3 +383,37 @@ def test_concurrent_mixed_calls_from_two_threads():
     for t in threads:
         t.join()
     assert not errors, errors
+
+
+@pytest.mark.parametrize("name", ["ragged", "long"])
+def test_bench_launch_configuration_sampled_rows(name):
+    """The configuration bench.py times: the full-size workload, the planned
+    split count, one call captured in a CUDA graph and replayed after an L2
+    flush; sampled rows (first and last of every request plus random ones)
+    against the oracle after each of two replays."""
+    from speculative_decode_mla_paged_gb300 import tuning
+
+    inp = W.make_config_inputs(name, device="cuda")
+    splits = tuning.plan_num_splits(inp.prefix_lens, inp.draft_lens, inp.num_heads)
+    d = device_inputs(inp)
+    runner = api.VerifyAttention(inp.batch, inp.max_q_per_req, inp.num_heads, splits)
+    out = torch.zeros(inp.total_q, inp.num_heads, 512, dtype=torch.bfloat16, device="cuda")
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
+    g = torch.cuda.CUDAGraph()
+    s = torch.cuda.Stream()
+    torch.cuda.synchronize()
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(g, stream=s):
+            runner(d["q"], d["kv_pool"], d["qo_indptr"], d["kv_indptr"], d["kv_indices"], d["out_cache_loc"],
+                   d["custom_mask"], d["mask_indptr"], inp.sm_scale, out)
+    host = inp
+    host.q, host.kv_pool = inp.q.cpu(), inp.kv_pool.cpu()
+    rows = sample_rows(host, n_random=32, seed=11)
+    ref = oracle_rows(host, rows)
+    for _ in range(2):
+        out.zero_()
+        flush.zero_()
+        g.replay()
+        torch.cuda.synchronize()
+        assert runner.status() == 0
+        assert_parity(as_rows(out)[rows], ref, f"{name}/graph/{splits} splits")
