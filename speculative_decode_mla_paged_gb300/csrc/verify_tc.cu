@@ -479,35 +479,57 @@ __device__ void s_softmax(const Params &p, Header *h, uint32_t smem, uint32_t tm
     const int64_t lr = u.r0 + r;
     const bool row_ok = lr < u.rows_b;
     const int64_t i = row_ok ? lr / H : 0;
-    const int64_t hh = row_ok ? lr % H : 0;
     // A negative scale is folded into Q (exact sign flips) so the score
     // scale below is >= 0 and the maximum of s is the maximum of s * scale.
     const uint32_t qsign = p.sm_scale < 0.f ? 0x80008000u : 0u;
     const float sl2 = fabsf(p.sm_scale) * LOG2E;
 
-    // Q row: dims 0..511 -> TMEM columns [0, 256) (column k/2 holds elements
-    // k, k+1; group 0 writes dims 0..255, group 1 dims 256..511); dims
-    // 512..575 -> shared memory, K-major 128-byte swizzled (group 1).
-    const __nv_bfloat16 *qrow = p.q + (u.qo0 + i) * p.q_stride_tok + hh * p.q_stride_head;
+    // Q rows: dims 0..511 -> TMEM columns [0, 256) (column k/2 holds
+    // elements k, k+1; group 0 writes dims 0..255, group 1 dims 256..511);
+    // dims 512..575 -> shared memory, K-major 128-byte swizzled (group 1).
+    // The loads are coalesced: for each 64-dim chunk, lanes 8s..8s+7 read
+    // the 128 contiguous bytes of row 4j + s of the warp's 32 rows (j = 0..7),
+    // so one instruction covers four rows; the chunk goes through a 4 KB
+    // per-warp stage (the P staging area, idle until the first tile; 16-B
+    // pieces swizzled by row so writes and reads avoid bank conflicts) and
+    // each thread then reads its own row for the TMEM store.
+    const int sub = lane >> 3, piece = lane & 7;
+    const __nv_bfloat16 *qsrc[8];      // row 4j + sub of this warp's 32 (null: past the request's rows)
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        const int64_t lrj = u.r0 + quad * 32 + 4 * j + sub;
+        qsrc[j] = lrj < u.rows_b ? p.q + (u.qo0 + lrj / H) * p.q_stride_tok + (lrj % H) * p.q_stride_head + piece * 8
+                                 : nullptr;
+    }
+    uint8_t *qst = reinterpret_cast<uint8_t *>(h) + S_STAGE + (uint32_t)warp * 4096u;
 #pragma unroll 1
     for (int c = grp * 4; c < grp * 4 + 4; ++c) {
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            uint4 x = make_uint4(0u, 0u, 0u, 0u);
+            if (qsrc[j] != nullptr) x = __ldg(reinterpret_cast<const uint4 *>(qsrc[j] + c * 64));
+            const int k = 4 * j + sub;
+            *reinterpret_cast<uint4 *>(qst + k * 128 + ((piece ^ (k & 7)) << 4)) = x;
+        }
+        __syncwarp();
         uint32_t w[32];
 #pragma unroll
         for (int v = 0; v < 8; ++v) {
-            uint4 x = make_uint4(0u, 0u, 0u, 0u);
-            if (row_ok) x = __ldg(reinterpret_cast<const uint4 *>(qrow + c * 64 + v * 8));
+            const uint4 x = *reinterpret_cast<const uint4 *>(qst + lane * 128 + ((v ^ (lane & 7)) << 4));
             w[4 * v] = x.x ^ qsign; w[4 * v + 1] = x.y ^ qsign; w[4 * v + 2] = x.z ^ qsign; w[4 * v + 3] = x.w ^ qsign;
         }
+        __syncwarp();                  // the next chunk reuses the stage
         tmem_st32(tmem + lane_base + 32u * (uint32_t)c, w);
     }
     if (grp == 1) {
-        uint8_t *qpe = reinterpret_cast<uint8_t *>(h) + S_QPE + (r >> 3) * 1024 + (r & 7) * 128;
 #pragma unroll
-        for (int v = 0; v < 8; ++v) {
+        for (int j = 0; j < 8; ++j) {
             uint4 x = make_uint4(0u, 0u, 0u, 0u);
-            if (row_ok) x = __ldg(reinterpret_cast<const uint4 *>(qrow + 512 + v * 8));
+            if (qsrc[j] != nullptr) x = __ldg(reinterpret_cast<const uint4 *>(qsrc[j] + 512));
             x.x ^= qsign; x.y ^= qsign; x.z ^= qsign; x.w ^= qsign;
-            *reinterpret_cast<uint4 *>(qpe + ((v ^ (r & 7)) << 4)) = x;
+            const int rr = quad * 32 + 4 * j + sub;
+            *reinterpret_cast<uint4 *>(reinterpret_cast<uint8_t *>(h) + S_QPE + (rr >> 3) * 1024 + (rr & 7) * 128 +
+                                       ((piece ^ (rr & 7)) << 4)) = x;
         }
         fence_proxy_async_smem();
     }
@@ -809,23 +831,40 @@ __device__ void o_rows(const Params &p, Header *h, uint32_t smem, uint32_t tmem,
     if (!__all_sync(0xffffffffu, wait_bar(h, smem_u32(&h->drain), 0u, p.status, false, false))) ok = false;
     if (!warp_wait(h, smem_u32(&h->l_ready), 0u, p.status, true)) ok = false;
     tc_fence_after_sync();
+    // O / l -> fp32 partial rows, 32 columns at a time.  Each warp stages its
+    // 32 rows x 32 columns in shared memory (the V ring, idle once the MMAs
+    // have drained; rows padded to 36 floats so the 16-B writes and reads
+    // below are free of bank conflicts) and writes them back four rows per
+    // instruction: lanes 8k..8k+7 store one row's 128 contiguous bytes,
+    // where a thread storing its own row would scatter 32 16-B pieces.
     const float il = h->inv_l[r];
-    const int64_t lr = u.r0 + r;
-    const int64_t row = u.qo0 * p.num_heads + lr;
-    const bool write = ok && lr < u.rows_b && row < p.rows_cap;
-    float *dst = p.part_o + ((int64_t)u.split * p.rows_cap + (write ? row : 0)) * DV;
+    float *stage = reinterpret_cast<float *>(reinterpret_cast<uint8_t *>(h) + O_VRING) + warp * 32 * 36;
+    const int sub = lane >> 3, col4 = (lane & 7) * 4;
+    float *dst[8];                    // row 4i + sub of this warp's 32, or null when not written
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const int64_t lr = u.r0 + warp * 32 + 4 * i + sub;
+        const int64_t row = u.qo0 * p.num_heads + lr;
+        dst[i] = ok && lr < u.rows_b && row < p.rows_cap ? p.part_o + ((int64_t)u.split * p.rows_cap + row) * DV + col4
+                                                         : nullptr;
+    }
 #pragma unroll 1
     for (int c = 0; c < DV / 32; ++c) {
         uint32_t v[32];
         tmem_ld32(tmem + lane_base + 32u * (uint32_t)c, v);
         tmem_ld_wait();
-        if (write) {
 #pragma unroll
-            for (int e = 0; e < 8; ++e)
-                *reinterpret_cast<float4 *>(dst + c * 32 + 4 * e) =
-                    make_float4(__uint_as_float(v[4 * e]) * il, __uint_as_float(v[4 * e + 1]) * il,
-                                __uint_as_float(v[4 * e + 2]) * il, __uint_as_float(v[4 * e + 3]) * il);
+        for (int e = 0; e < 8; ++e)
+            *reinterpret_cast<float4 *>(stage + lane * 36 + 4 * e) =
+                make_float4(__uint_as_float(v[4 * e]) * il, __uint_as_float(v[4 * e + 1]) * il,
+                            __uint_as_float(v[4 * e + 2]) * il, __uint_as_float(v[4 * e + 3]) * il);
+        __syncwarp();
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const float4 x = *reinterpret_cast<const float4 *>(stage + (4 * i + sub) * 36 + col4);
+            if (dst[i] != nullptr) *reinterpret_cast<float4 *>(dst[i] + c * 32) = x;
         }
+        __syncwarp();                 // the next chunk reuses the stage
     }
 }
 
