@@ -73,10 +73,19 @@ def load_peaks():
     return dict(FALLBACK_PEAKS), "fallback"
 
 
-def default_splits(cfg_name, inp, kernel):
-    """Split count planned from this workload's lengths (host-side simulation of the grid)."""
-    from speculative_decode_mla_paged_gb300 import tuning
-    return tuning.plan_num_splits(inp.prefix_lens, inp.draft_lens, inp.num_heads, kernel)
+def choose_splits(inp, d, kernel):
+    """Split count for this workload and how it was chosen: the tensor-core
+    path times the four best candidates of the grid simulation as cold
+    CUDA-graph replays (api.tune_num_splits) and keeps the fastest; the
+    CUDA-core path takes the simulation's pick."""
+    from speculative_decode_mla_paged_gb300 import api, tuning
+    if kernel != "tc":
+        return tuning.plan_num_splits(inp.prefix_lens, inp.draft_lens, inp.num_heads, kernel), "simulated"
+    cands = tuning.ranked_num_splits(inp.prefix_lens, inp.draft_lens, inp.num_heads, k=4)
+    s = api.tune_num_splits(d["q"], d["kv_pool"], d["qo_indptr"], d["kv_indptr"], d["kv_indices"],
+                            d["out_cache_loc"], d["custom_mask"], d["mask_indptr"], inp.sm_scale, d["out"],
+                            inp.max_q_per_req, cands)
+    return s, f"fastest of {cands} timed as graph replays (simulated ranking)"
 
 
 def code_text(src: str) -> str:
@@ -394,8 +403,8 @@ def run_ours(args):
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
 
     inp = W.make_config_inputs(args.config, device=dev)
-    splits = args.num_splits or default_splits(args.config, inp, args.kernel)
     d = device_tensors(inp, torch, dev)
+    splits, split_choice = (args.num_splits, "given") if args.num_splits else choose_splits(inp, d, args.kernel)
     runner = api.VerifyAttention(inp.batch, inp.max_q_per_req, inp.num_heads, splits, impl=args.kernel)
 
     # ---- device-resident timed region
@@ -476,7 +485,7 @@ def run_ours(args):
         "warmup": args.warmup, "ms_per_step": t_total_ms / args.steps, "higher_is_better": False,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {"workload": f"{args.config}: {W.CONFIGS[args.config].description}",
-                   "kernel": args.kernel, "num_splits": splits,
+                   "kernel": args.kernel, "num_splits": splits, "num_splits_choice": split_choice,
                    "timing": "cold replays of one call captured in a CUDA graph",
                    "l2": "flushed before every timed replay (256 MiB write, excluded from timing)",
                    "parallelism": "replicas" if world > 1 else "single-gpu"},
@@ -501,8 +510,8 @@ def run_ours(args):
         table = {}
         for name in W.CONFIG_ORDER + W.EXTRA_CONFIG_ORDER:
             ci = inp if name == args.config else W.make_config_inputs(name, device=dev)
-            cs = args.num_splits or default_splits(name, ci, args.kernel)
             cd = d if name == args.config else device_tensors(ci, torch, dev)
+            cs = splits if name == args.config else (args.num_splits or choose_splits(ci, cd, args.kernel)[0])
             cr = runner if name == args.config else api.VerifyAttention(ci.batch, ci.max_q_per_req,
                                                                           ci.num_heads, cs, impl=args.kernel)
             cm, sm, _ = measure(ci, cd, cr, 5, 3, flush, torch)

@@ -203,6 +203,49 @@ def read_status(workspace: torch.Tensor) -> int:
     return int(workspace[:4].view(torch.int32).item()) & 0xFFFFFFFF
 
 
+def tune_num_splits(q: torch.Tensor, kv_pool: torch.Tensor, qo_indptr: torch.Tensor, kv_indptr: torch.Tensor,
+                    kv_indices: torch.Tensor, out_cache_loc: torch.Tensor, custom_mask: torch.Tensor,
+                    mask_indptr: torch.Tensor, sm_scale: float, out: torch.Tensor, max_q_per_req: int,
+                    candidates, impl: str = "tc", replays: int = 6, flush_bytes: int = 256 << 20) -> int:
+    """The fastest of `candidates` (split counts) for this call, timed as a
+    serving loop runs it: one call captured in a CUDA graph and replayed,
+    L2 flushed (a `flush_bytes` write) before each replay, CUDA events around
+    it; the median of `replays` after one warm-up replay.  Allocates a
+    workspace per candidate and the flush buffer, so run it once per
+    workload shape, outside any capture; `out` is overwritten."""
+    num_heads = q.shape[1]
+    batch = qo_indptr.numel() - 1
+    flush = torch.empty(flush_bytes, dtype=torch.uint8, device=q.device)
+    best, best_s = None, None
+    for s in candidates:
+        run = VerifyAttention(batch, max_q_per_req, num_heads, int(s), device=q.device, impl=impl)
+        args = (q, kv_pool, qo_indptr, kv_indptr, kv_indices, out_cache_loc, custom_mask, mask_indptr, sm_scale, out)
+        run(*args)
+        torch.cuda.synchronize(q.device)
+        graph, stream = torch.cuda.CUDAGraph(), torch.cuda.Stream(q.device)
+        with torch.cuda.stream(stream):
+            with torch.cuda.graph(graph, stream=stream):
+                run(*args)
+        torch.cuda.synchronize(q.device)
+        times = []
+        for k in range(replays + 1):
+            flush.zero_()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            graph.replay()
+            e1.record()
+            e1.synchronize()
+            if k > 0:
+                times.append(e0.elapsed_time(e1))
+        if run.status() != 0:
+            raise VerifyAttnError(f"tune_num_splits: device status {run.status():#x} with {s} splits")
+        t = sorted(times)[len(times) // 2]
+        if best is None or t < best:
+            best, best_s = t, int(s)
+        del graph, run
+    return best_s
+
+
 class VerifyAttention:
     """Holds a workspace sized for fixed capacities and runs the call.
 

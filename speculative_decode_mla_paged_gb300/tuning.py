@@ -73,18 +73,39 @@ def simulate(prefix_lens: Sequence[int], draft_lens: Sequence[int], num_heads: i
     return finish + combine
 
 
-def plan_num_splits(prefix_lens: Sequence[int], draft_lens: Sequence[int], num_heads: int,
-                    kernel: str = "tc") -> int:
-    """The candidate split count with the smallest simulated time."""
+def _candidates(prefix_lens: Sequence[int], draft_lens: Sequence[int]):
+    """Split counts worth simulating: every candidate up to the point where a
+    larger count no longer changes the longest request's chunk."""
     n_max = max(int(l) + int(t) for l, t in zip(prefix_lens, draft_lens))
-    best, best_s = None, 1
     for s in CANDIDATES:
         if s > 1 and split_chunk(n_max, s) == split_chunk(n_max, s - 1) and s > n_max // MIN_CHUNK + 1:
             break
+        yield s
+
+
+def plan_num_splits(prefix_lens: Sequence[int], draft_lens: Sequence[int], num_heads: int,
+                    kernel: str = "tc") -> int:
+    """The candidate split count with the smallest simulated time."""
+    best, best_s = None, 1
+    for s in _candidates(prefix_lens, draft_lens):
         cost = simulate(prefix_lens, draft_lens, num_heads, s, kernel)
         if best is None or cost < best * 0.98:
             best, best_s = cost, s
     return best_s
+
+
+def ranked_num_splits(prefix_lens: Sequence[int], draft_lens: Sequence[int], num_heads: int, k: int = 4,
+                      kernel: str = "tc") -> list:
+    """The k candidate split counts with the smallest simulated times, best
+    first (the planner's pick leads).  The simulation tracks measured times
+    closely for calls of one cluster shape; when a call runs both shapes the
+    two grids interleave in ways it does not model, so these are candidates
+    to time (``api.tune_num_splits``), not an answer."""
+    costs = sorted((simulate(prefix_lens, draft_lens, num_heads, s, kernel), s)
+                   for s in _candidates(prefix_lens, draft_lens))
+    plan = plan_num_splits(prefix_lens, draft_lens, num_heads, kernel)
+    out = [plan] + [s for _, s in costs if s != plan]
+    return out[:max(1, k)]
 
 
 def default_num_splits(batch: int, max_q_per_req: int, num_heads: int, max_keys: int,

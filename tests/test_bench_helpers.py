@@ -31,3 +31,16 @@ def test_launches_per_call():
     assert bench.launches_per_call(cfg(1, 16), "tc") == 2
     assert bench.launches_per_call(cfg(64, 256), "tc") == 2     # every request above one tile
     assert bench.launches_per_call(cfg(64, 8), "simt") == 2
+
+
+def test_ranked_num_splits_leads_with_the_plan():
+    import numpy as np
+
+    from speculative_decode_mla_paged_gb300 import tuning, workloads as W
+
+    for name in ("ragged", "long", "decode", "short"):
+        cfg = W.CONFIGS[name]
+        prefix, drafts = W.draw_lengths(cfg, np.random.Generator(np.random.PCG64(cfg.seed + 7919)))
+        r = tuning.ranked_num_splits(prefix, drafts, cfg.num_heads, k=4)
+        assert r[0] == tuning.plan_num_splits(prefix, drafts, cfg.num_heads)
+        assert 1 <= len(r) <= 4 and len(set(r)) == len(r)
