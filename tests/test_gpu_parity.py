@@ -421,3 +421,23 @@ def test_bench_launch_configuration_sampled_rows(name):
             assert runner.status() == 0
             assert_parity(as_rows(out)[rows], ref, f"{name}/graph/{splits} splits")
         del g, runner
+
+def test_tune_num_splits_returns_a_candidate_and_a_correct_call():
+    """api.tune_num_splits times each candidate as graph replays of the real
+    (here mixed-shape) call and returns one of them; the output it leaves
+    matches the oracle, and a runner at the chosen count agrees."""
+    from speculative_decode_mla_paged_gb300 import tuning
+
+    inp = W.make_inputs([2500, 700, 90], [24, 8, 16], 8, 8192, seed=91)
+    d = device_inputs(inp)
+    out = torch.zeros(inp.total_q, inp.num_heads, 512, dtype=torch.bfloat16, device="cuda")
+    cands = tuning.ranked_num_splits(inp.prefix_lens, inp.draft_lens, inp.num_heads, k=3)
+    s = api.tune_num_splits(d["q"], d["kv_pool"], d["qo_indptr"], d["kv_indptr"], d["kv_indices"],
+                            d["out_cache_loc"], d["custom_mask"], d["mask_indptr"], inp.sm_scale, out,
+                            inp.max_q_per_req, cands, replays=2, flush_bytes=8 << 20)
+    assert s in cands
+    ref = oracle_rows(inp)
+    assert_parity(as_rows(out), ref, "after tuning")
+    got, status = run(inp, num_splits=s)
+    assert status == 0
+    assert_parity(as_rows(got), ref, f"tuned {s} splits")
