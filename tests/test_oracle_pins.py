@@ -348,3 +348,18 @@ def test_save_kv_oracle_replaces_exactly_the_named_rows():
         oracle.save_kv(pool, np.array([1, 1]), new[:2])
     with pytest.raises(ValueError):
         oracle.save_kv(pool, np.array([50]), new[:1])
+
+
+def test_thread_count_does_not_change_results():
+    """Rows are independent: one thread and all threads give bit-identical
+    outputs (the bench times the oracle both ways)."""
+    inp = W.make_inputs([300, 40, 0], [8, 5, 3], num_heads=4, pool_size=512, seed=12)
+    n = oracle.num_threads()
+    try:
+        oracle.set_num_threads(1)
+        assert oracle.num_threads() == 1
+        out1, lse1 = oracle.run(inp)
+    finally:
+        oracle.set_num_threads(n)
+    outn, lsen = oracle.run(inp)
+    assert np.array_equal(out1, outn) and np.array_equal(lse1, lsen)
