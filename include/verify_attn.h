@@ -52,6 +52,12 @@
  * calls must use distinct workspaces.  Mixed-shape calls on one device share
  * the library's second stream (a lock keeps each call's fork, launch and
  * join together), so their small-request launches run one after another.
+ * A stream capture that has recorded a mixed-shape call holds that second
+ * stream until the capture ends (the forked stream belongs to the capture):
+ * on that device, make no mixed-shape call from another thread meanwhile.
+ * Such a call is not supported.  Its fork would wait from a capturing
+ * stream on an event recorded outside the capture, so the call can fail
+ * with VA_ERR_LAUNCH and invalidate the capture.
  */
 #ifndef VERIFY_ATTN_H
 #define VERIFY_ATTN_H
