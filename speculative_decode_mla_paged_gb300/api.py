@@ -296,16 +296,20 @@ class VerifyAttention:
         if self._check_ws is None:
             self._check_ws = torch.empty_like(self.workspace)
         other = "simt" if self.impl == "tc" else "tc"
-        ref = torch.empty_like(out)
-        verify_attn(q, kv_pool, qo_indptr, kv_indptr, kv_indices, out_cache_loc, custom_mask, mask_indptr,
-                    sm_scale, out=ref, workspace=self._check_ws, max_q_per_req=self.max_q_per_req,
-                    num_splits=self.num_splits, impl=other, stream=stream)
-        a, b = out.float(), ref.float()
-        diff = (a - b).abs()
-        excess = diff - (self.atol + self.rtol * b.abs())
-        rec = {"against": other, "max_abs_diff": float(diff.max()) if diff.numel() else 0.0,
-               "max_excess": float(excess.max()) if excess.numel() else float("-inf"),
-               "status": read_status(self.workspace), "check_status": read_status(self._check_ws)}
+        # The comparison runs on the stream both kernels ran on, so its reads
+        # (and the synchronising .item() calls) come after them.
+        s = stream if stream is not None else torch.cuda.current_stream(out.device)
+        with torch.cuda.stream(s):
+            ref = torch.empty_like(out)
+            verify_attn(q, kv_pool, qo_indptr, kv_indptr, kv_indices, out_cache_loc, custom_mask, mask_indptr,
+                        sm_scale, out=ref, workspace=self._check_ws, max_q_per_req=self.max_q_per_req,
+                        num_splits=self.num_splits, impl=other, stream=s)
+            a, b = out.float(), ref.float()
+            diff = (a - b).abs()
+            excess = diff - (self.atol + self.rtol * b.abs())
+            rec = {"against": other, "max_abs_diff": float(diff.max()) if diff.numel() else 0.0,
+                   "max_excess": float(excess.max()) if excess.numel() else float("-inf"),
+                   "status": read_status(self.workspace), "check_status": read_status(self._check_ws)}
         rec["ok"] = bool(rec["max_excess"] <= 0 and rec["status"] == 0 and rec["check_status"] == 0)
         self.last_validation = rec
         if not rec["ok"]:

@@ -60,3 +60,20 @@ def test_validate_mode_flags_a_mismatch():
         runner._cross_check(d["q"], d["kv_pool"], d["qo_indptr"], d["kv_indptr"], d["kv_indices"],
                             d["out_cache_loc"], d["custom_mask"], d["mask_indptr"], inp.sm_scale, out, None)
     assert not runner.last_validation["ok"]
+
+
+def test_validate_mode_on_a_stream_that_is_not_current():
+    """With an explicit stream both kernels and the comparison run on it, so
+    the check reads finished outputs."""
+    inp = W.make_config_inputs("mid", device="cuda")
+    d = _dev(inp)
+    out = torch.empty((inp.total_q, inp.num_heads, W.V_DIM), dtype=torch.bfloat16, device="cuda")
+    runner = api.VerifyAttention(inp.batch, inp.max_q_per_req, inp.num_heads, 8, validate=True)
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    runner(d["q"], d["kv_pool"], d["qo_indptr"], d["kv_indptr"], d["kv_indices"], d["out_cache_loc"],
+           d["custom_mask"], d["mask_indptr"], inp.sm_scale, out, stream=side)
+    rec = runner.last_validation
+    assert rec["ok"], rec
+    torch.cuda.current_stream().wait_stream(side)
+    assert runner.status() == 0
