@@ -140,12 +140,13 @@ class VerifyInputs:
         return int(bits[: int(self.mask_indptr[-1])].sum()) * self.num_heads
 
     def algorithmic_bytes(self) -> int:
-        """Each KV row once + q + out + indices + mask + indptrs."""
+        """Each KV row once + q + out + indices + mask + indptrs (qo_indptr and
+        kv_indptr int32, mask_indptr int64)."""
         n_keys = int(self.kv_indptr[-1]) + int(self.qo_indptr[-1])
         rows = self.total_q * self.num_heads
         return (n_keys * LATENT_DIM * 2 + rows * LATENT_DIM * 2 + rows * V_DIM * 2
                 + int(self.kv_indptr[-1]) * 4 + self.total_q * 8
-                + (int(self.mask_indptr[-1]) + 7) // 8 + 3 * (self.batch + 1) * 8)
+                + (int(self.mask_indptr[-1]) + 7) // 8 + (self.batch + 1) * (4 + 4 + 8))
 
     def algorithmic_flops(self) -> int:
         """2*(576+512) flops per visible (row, key) pair."""
