@@ -21,6 +21,13 @@ MUTATIONS = {
     "no_sm_scale": ("double s = a->sm_scale * dot;", "double s = dot;"),
     "ignore_mask_indptr": ("a->mask_indptr[b] + i * N + j", "i * N + j"),
     "softmax_sign": ("double w = exp(scores[j - k0] - m);", "double w = exp(m - scores[j - k0]);"),
+    "mask_row_stride_prefix_len": ("a->mask_indptr[b] + i * N + j", "a->mask_indptr[b] + i * L + j"),
+    "draft_slot_without_request_offset": ("return a->out_cache_loc[a->qo_indptr[b] + (j - L)];",
+                                          "return a->out_cache_loc[j - L];"),
+    "q_head_stride_dropped": ("+ (int64_t)h * a->q_stride_head;", "+ (int64_t)h * 0;"),
+    "max_not_subtracted": ("double w = exp(scores[j - k0] - m);", "double w = exp(scores[j - k0]);"),
+    "lse_in_log2": ("*lse_out = m + log(z);", "*lse_out = m + log2(z);"),
+    "splits_averaged_equally": ("double w = exp(plse[s] - mx);", "double w = 1.0;"),
 }
 
 
