@@ -108,6 +108,7 @@ RAGGED_CASES = {
     "empty_requests": ([10, 0, 77, 5], [0, 4, 0, 2], 4),
     "drafts_only": ([0, 0], [6, 11], 8),
     "many_rows": ([300], [64], 16),
+    "wide_heads": ([300, 50, 0], [3, 2, 4], 160),   # H > 128: one token's heads span row tiles
 }
 
 
