@@ -9,6 +9,12 @@
 #include <atomic>
 #include <math.h>
 
+// The ABI's constants and the kernels' own must agree.
+static_assert(va::D == VERIFY_ATTN_LATENT_DIM && va::DV == VERIFY_ATTN_V_DIM, "latent row and V widths");
+static_assert(va::STATUS_BAD_SLOT == VA_STATUS_BAD_SLOT && va::STATUS_BAD_META == VA_STATUS_BAD_META &&
+                  va::STATUS_TIMEOUT == VA_STATUS_TIMEOUT,
+              "device status bits");
+
 namespace va {
 
 cudaError_t tc_init();

@@ -2,6 +2,7 @@
 symbol, sizes workspaces, and rejects bad host arguments before any CUDA call."""
 import ctypes
 import math
+import re
 
 import pytest
 
@@ -32,10 +33,27 @@ def test_workspace_size_layout(lib):
     assert lib.verify_attn_workspace_size(1, 8, 8, 257) == 0
 
 
+def _header_text():
+    return open(api.HEADER).read()
+
+
 def test_status_strings(lib):
-    for code in range(-8, 1):
+    codes = {name: int(v) for name, v in re.findall(r"\b(VA_ERR_\w+)\s*=\s*(-\d+)", _header_text())}
+    assert len(codes) >= 9 and sorted(codes.values()) == list(range(-len(codes), 0))
+    for code in [0] + list(codes.values()):
         assert api.status_string(code) != "unknown status"
     assert api.status_string(-99) == "unknown status"
+
+
+def test_binding_constants_match_the_header():
+    defs = {k: int(v, 0) for k, v in re.findall(r"#define\s+(\w+)\s+(0x[0-9a-fA-F]+|\d+)u?\b", _header_text())}
+    assert defs["VERIFY_ATTN_LATENT_DIM"] == api.LATENT_DIM == 576
+    assert defs["VERIFY_ATTN_V_DIM"] == api.V_DIM == 512
+    assert defs["VERIFY_ATTN_MAX_SPLITS"] == api.MAX_SPLITS
+    assert defs["VA_STATUS_BAD_SLOT"] == api.STATUS_BAD_SLOT
+    assert defs["VA_STATUS_BAD_META"] == api.STATUS_BAD_META
+    assert defs["VA_STATUS_TIMEOUT"] == api.STATUS_TIMEOUT
+    assert (defs["VERIFY_ATTN_IMPL_TC"], defs["VERIFY_ATTN_IMPL_SIMT"]) == (0, 1)
 
 
 A = 0x100000  # a fake, well-aligned device address: never dereferenced on the host path
