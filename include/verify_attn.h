@@ -134,6 +134,9 @@ VERIFY_ATTN_API int verify_attn_init(void);
  *                q[t*q_stride_tok + h*q_stride_head + d]; strides in
  *                elements, multiples of 8; 16-B aligned base.
  *   kv_pool      [pool_size, 576] bf16, rows contiguous (1152 B), 16-B aligned.
+ *                The tensor-core kernel addresses rows with 32-bit TMA
+ *                coordinates, so a pool of 2^31 rows or more (2.5 TB, more
+ *                than one GPU holds) runs on the CUDA-core kernel instead.
  *   qo_indptr    [batch+1] int32, non-decreasing, qo_indptr[0] = 0, every
  *                T_b <= max_q_per_req.
  *   kv_indptr    [batch+1] int32, non-decreasing, kv_indptr[0] = 0 (prefix keys).
