@@ -44,6 +44,7 @@ UNIT = "us/call"
 HEADLINE = "ragged"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 L2_FLUSH_BYTES = 256 << 20
+CLOCK_HOLD_S = 1.0          # the timed replays' load is held this long for the 200 ms clock sampler
 KERNEL_SOURCES = {"tc": "speculative_decode_mla_paged_gb300/csrc/verify_tc.cu",
                   "simt": "speculative_decode_mla_paged_gb300/csrc/verify_simt.cu"}
 
@@ -160,7 +161,9 @@ class ClockSampler:
         for line in self.proc.stdout:
             self.lines.append((time.time(), line.strip()))
 
-    def stop(self):
+    def stop(self, window=None):
+        """Stop sampling; summarise the samples read inside `window` = (t0, t1)
+        (wall-clock seconds), or all of them when no window is given."""
         if self.proc is None:
             return None
         time.sleep(0.25)
@@ -169,23 +172,43 @@ class ClockSampler:
             self.proc.wait(timeout=5)
         except subprocess.TimeoutExpired:
             self.proc.kill()
-        sm, mx, reasons = [], [], set()
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for _, line in self.lines:
-            parts = [x.strip() for x in line.split(",")]
-            if len(parts) < 9:
-                continue
-            try:
-                sm.append(float(parts[1])); mx.append(float(parts[2]))
-            except ValueError:
-                continue
-            for n, v in zip(names, parts[5:9]):
-                if v.lower().startswith("active"):
-                    reasons.add(n)
-        if not sm:
-            return None
-        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
-                "samples": len(sm)}
+        return summarise_clocks(self.lines, window)
+
+
+def _clock_stats(lines):
+    sm, mx, reasons = [], [], set()
+    names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+    for _, line in lines:
+        parts = [x.strip() for x in line.split(",")]
+        if len(parts) < 9:
+            continue
+        try:
+            sm.append(float(parts[1])); mx.append(float(parts[2]))
+        except ValueError:
+            continue
+        for n, v in zip(names, parts[5:9]):
+            if v.lower().startswith("active"):
+                reasons.add(n)
+    if not sm:
+        return None
+    return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def summarise_clocks(lines, window=None):
+    """Median SM clock, max clock and throttle reasons of nvidia-smi CSV lines
+    [(read time, text)].  With a load `window` = (t0, t1) only the lines read
+    inside it (its end stretched by one 200 ms period) count, and `window_s`
+    gives its length; if no line was read inside it (output that reached the
+    pipe late), every line counts and `window_s` is null."""
+    if window is not None:
+        out = _clock_stats([(ts, ln) for ts, ln in lines if window[0] <= ts <= window[1] + 0.2])
+        if out is not None:
+            out["window_s"] = round(window[1] - window[0], 3)
+            return out
+    out = _clock_stats(lines)
+    if out is not None and window is not None:
+        out["window_s"] = None
+    return out
 
 
 def dist_setup(args):
@@ -345,11 +368,14 @@ def measure_warm(inp, d, runner, steps, torch):
     return e0.elapsed_time(e1) / steps
 
 
-def measure_graph(inp, d, runner, steps, warmup, flush, torch):
+def measure_graph(inp, d, runner, steps, warmup, flush, torch, hold_s=0.0):
     """Cold replays of one call captured in a CUDA graph (how a serving loop
     runs it), each after an L2 flush outside the timed events.  The library
-    records its phase events inside the graph.  Returns per-replay lists of
-    (replay_ms, split_ms, combine_ms)."""
+    records its phase events inside the graph.  After the timed replays the
+    same flush + replay pairs go on, untimed and synchronised one by one,
+    until the load has lasted `hold_s` seconds, so that a clock sampler with a
+    200 ms period sees the GPU under this load.  Returns per-replay lists of
+    (replay_ms, split_ms, combine_ms) and the load's wall-clock window."""
     inner = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
     for e in inner:                     # create the CUDA events before the capture
         e.record()
@@ -362,6 +388,7 @@ def measure_graph(inp, d, runner, steps, warmup, flush, torch):
                    d["custom_mask"], d["mask_indptr"], inp.sm_scale, d["out"], events=inner)
     torch.cuda.synchronize()
     call_ms, split_ms, comb_ms = [], [], []
+    t_load = time.time()
     for k in range(warmup + steps):
         flush.zero_()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -373,7 +400,11 @@ def measure_graph(inp, d, runner, steps, warmup, flush, torch):
             call_ms.append(e0.elapsed_time(e1))
             split_ms.append(inner[1].elapsed_time(inner[2]))
             comb_ms.append(inner[2].elapsed_time(inner[3]))
-    return call_ms, split_ms, comb_ms
+    while time.time() - t_load < hold_s:
+        flush.zero_()
+        g.replay()
+        torch.cuda.synchronize()
+    return call_ms, split_ms, comb_ms, (t_load, time.time())
 
 
 def device_tensors(inp, torch, dev):
@@ -420,8 +451,9 @@ def run_ours(args):
     sampler = ClockSampler(gpu_index)
     sampler.start()
     time.sleep(0.3)
-    call_ms, split_ms, comb_ms = measure_graph(inp, d, runner, args.steps, args.warmup, flush, torch)
-    clocks = sampler.stop()
+    call_ms, split_ms, comb_ms, load_window = measure_graph(inp, d, runner, args.steps, args.warmup, flush, torch,
+                                                           hold_s=CLOCK_HOLD_S)
+    clocks = sampler.stop(load_window)
     status = runner.status()
     if status != 0:
         raise RuntimeError(f"device status word {status:#x}")
