@@ -51,3 +51,16 @@ def test_per_call_us_counts_all_replicas():
 def test_single_rank_needs_no_process_group():
     assert not dist.is_initialized()
     assert bench.max_over_ranks(7.0, 1) == 7.0
+
+
+def test_reference_arm_runs_on_rank_zero_only():
+    """Under torchrun only rank 0 times the oracle and prints the line; any
+    other rank exits 0 at once, printing nothing."""
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    env = dict(os.environ, RANK="1", WORLD_SIZE="2", LOCAL_RANK="1", MASTER_ADDR="127.0.0.1")
+    r = subprocess.run([sys.executable, os.path.join(root, "bench.py"), "--impl", "reference", "--gpus", "2"],
+                       cwd=root, env=env, capture_output=True, text=True, timeout=120)
+    assert r.returncode == 0, r.stderr[-2000:]
+    assert r.stdout.strip() == ""
