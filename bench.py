@@ -16,10 +16,13 @@ end from pinned host buffers.  Prints ONE JSON line.
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
                   [--config ragged|long|mid|short|tiny] [--kernel tc|simt]
 
-Under torchrun (N > 1) every rank runs an independent replica of the same
-workload (this path has no cross-GPU exchange); the value is the whole-job
-time per call, max over ranks.  ``--impl reference`` times the CPU oracle on
-the host cores (rank 0 only).
+The path runs on one GPU.  More than one GPU (``--gpus N > 1`` or a torchrun
+world larger than one) is refused before CUDA is touched: rank 0 prints a
+JSON line with an ``unavailable`` reason, every rank exits 0, and nothing is
+launched.  The tensor-core kernel's 4-CTA clusters issue TMA loads with
+cluster multicast, which this library keeps to single-GPU calls.
+``--impl reference`` times the CPU oracle on the host cores (rank 0 only;
+other ranks exit 0 at once).
 """
 from __future__ import annotations
 
@@ -60,6 +63,8 @@ def parse_args():
     ap.add_argument("--num-splits", type=int, default=0, help="0 = per-config default")
     ap.add_argument("--no-per-config", action="store_true", help="skip the five-config table")
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="oracle sample budget")
+    ap.add_argument("--launch-only", action="store_true",
+                    help="for profilers: W warm-up and K timed direct calls of the workload, nothing else")
     return ap.parse_args()
 
 
@@ -417,18 +422,45 @@ def device_tensors(inp, torch, dev):
     return d
 
 
+def run_launch_only(args):
+    """W warm-up and K direct calls of one workload (L2 flushed before each),
+    with no split-count timing, graph, end-to-end or oracle work around them,
+    so that a profiler's launch list is just these calls: 2 or 3 library
+    launches per call (the split kernel(s) and the combine)."""
+    import torch
+
+    from speculative_decode_mla_paged_gb300 import api, tuning
+    from speculative_decode_mla_paged_gb300 import workloads as W
+
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    api.init()
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    inp = W.make_config_inputs(args.config, device=dev)
+    d = device_tensors(inp, torch, dev)
+    splits = args.num_splits or tuning.plan_num_splits(inp.prefix_lens, inp.draft_lens, inp.num_heads,
+                                                       args.kernel)
+    runner = api.VerifyAttention(inp.batch, inp.max_q_per_req, inp.num_heads, splits, impl=args.kernel)
+    call_ms, split_ms, _ = measure(inp, d, runner, args.steps, args.warmup, flush, torch)
+    status = runner.status()
+    print(json.dumps({"mode": "launch-only", "config": args.config, "kernel": args.kernel, "num_splits": splits,
+                      "steps": args.steps, "warmup": args.warmup, "status": status,
+                      "us_per_call": statistics.mean(call_ms) * 1e3, "split_us": statistics.mean(split_ms) * 1e3,
+                      "launches_per_call": launches_per_call(inp, args.kernel)}), flush=True)
+    if status != 0:
+        raise SystemExit(f"device status word {status:#x}")
+
+
 def run_ours(args):
     import torch
-    import torch.distributed as dist
 
     from speculative_decode_mla_paged_gb300 import api
     from speculative_decode_mla_paged_gb300 import workloads as W
 
     world, rank, local = dist_setup(args)
+    assert world == 1, "multi-GPU runs are refused in main() before CUDA is touched"
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
-    if world > 1:
-        dist.init_process_group("nccl", device_id=dev)
     api.init()
     peaks, peak_src = load_peaks()
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
@@ -439,8 +471,6 @@ def run_ours(args):
     runner = api.VerifyAttention(inp.batch, inp.max_q_per_req, inp.num_heads, splits, impl=args.kernel)
 
     # ---- device-resident timed region
-    if world > 1:
-        dist.barrier()
     torch.cuda.synchronize()
     gpu_index = None
     try:
@@ -520,7 +550,7 @@ def run_ours(args):
                    "kernel": args.kernel, "num_splits": splits, "num_splits_choice": split_choice,
                    "timing": "cold replays of one call captured in a CUDA graph",
                    "l2": "flushed before every timed replay (256 MiB write, excluded from timing)",
-                   "parallelism": "replicas" if world > 1 else "single-gpu"},
+                   "parallelism": "single-gpu"},
         "tflops": flops / call_s / 1e12, "kv_gbs": nbytes / call_s / 1e9,
         "roofline_frac_call": max(t_f, t_b) / call_s,
         "split_us": statistics.mean(split_ms) * 1e3, "combine_us": statistics.mean(comb_ms) * 1e3,
@@ -576,16 +606,33 @@ def run_ours(args):
         line["cpu_baseline"]["single_core"] = {
             "value": us1, "unit": UNIT, "cores": 1,
             "sample": f"{sample1['rows']} output rows ({sample1['seconds']} s), scaled the same way"}
+    print(json.dumps(line), flush=True)
+
+
+MULTI_GPU_REFUSAL = ("single-GPU path: the tensor-core kernel's 4-CTA clusters use cluster-multicast TMA "
+                     "loads, which this library runs on single-GPU calls only; no launch was made")
+
+
+def refuse_multi_gpu(args):
+    """True (after rank 0 printed the refusal line) when the run asks for more
+    than one GPU.  Called before anything touches CUDA."""
+    world, rank, _ = dist_setup(args)
+    if world <= 1 and args.gpus <= 1:
+        return False
     if rank == 0:
-        print(json.dumps(line), flush=True)
-    if world > 1:
-        dist.destroy_process_group()
+        print(json.dumps({"metric": METRIC, "n_gpus": max(world, args.gpus), "unit": UNIT,
+                          "unavailable": MULTI_GPU_REFUSAL}), flush=True)
+    return True
 
 
 def main():
     args = parse_args()
+    if args.impl != "reference" and refuse_multi_gpu(args):
+        return
     if args.impl == "reference":
         run_reference(args)
+    elif args.launch_only:
+        run_launch_only(args)
     else:
         run_ours(args)
 

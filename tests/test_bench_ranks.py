@@ -64,3 +64,44 @@ def test_reference_arm_runs_on_rank_zero_only():
                        cwd=root, env=env, capture_output=True, text=True, timeout=120)
     assert r.returncode == 0, r.stderr[-2000:]
     assert r.stdout.strip() == ""
+
+
+def _bench_env(rank, world):
+    return dict(os.environ, RANK=str(rank), WORLD_SIZE=str(world), LOCAL_RANK=str(rank),
+                MASTER_ADDR="127.0.0.1", CUDA_VISIBLE_DEVICES="")
+
+
+@pytest.mark.parametrize("rank", [0, 1])
+def test_our_arm_refuses_more_than_one_gpu_before_cuda(rank):
+    """Under a torchrun world of two, bench.py's own arm launches nothing: the
+    tensor-core kernel's cluster-multicast loads stay on single-GPU calls.
+    Rank 0 prints one JSON line with the reason, rank 1 prints nothing, both
+    exit 0, and neither imports the library's binding or initialises CUDA
+    (the subprocess sees no devices, so any CUDA use would fail)."""
+    import json
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    probe = ("import sys, runpy; sys.argv = ['bench.py', '--gpus', '2']; "
+             "runpy.run_path('bench.py', run_name='__main__'); "
+             "import torch; assert not torch.cuda.is_initialized(); "
+             "assert 'speculative_decode_mla_paged_gb300.api' not in sys.modules")
+    r = subprocess.run([sys.executable, "-c", probe], cwd=root, env=_bench_env(rank, 2),
+                       capture_output=True, text=True, timeout=120)
+    assert r.returncode == 0, r.stderr[-2000:]
+    if rank == 0:
+        line = json.loads(r.stdout.strip())
+        assert line["n_gpus"] == 2 and "multicast" in line["unavailable"]
+    else:
+        assert r.stdout.strip() == ""
+
+
+def test_gpus_flag_alone_is_refused_too():
+    import json
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    r = subprocess.run([sys.executable, os.path.join(root, "bench.py"), "--gpus", "4"], cwd=root,
+                       env=_bench_env(0, 1), capture_output=True, text=True, timeout=120)
+    assert r.returncode == 0, r.stderr[-2000:]
+    assert json.loads(r.stdout.strip())["n_gpus"] == 4
