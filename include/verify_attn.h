@@ -119,10 +119,13 @@ enum verify_attn_status {
 VERIFY_ATTN_API size_t verify_attn_workspace_size(int batch, int max_q_per_req, int num_heads, int num_splits);
 
 /*
- * One-time per-device setup for the current device (kernel attributes such
- * as the dynamic shared-memory limit).  verify_attn_run calls it lazily, but
- * callers that capture CUDA graphs should call it once before capturing.
- * Returns VA_OK, VA_ERR_DEVICE or VA_ERR_LAUNCH.
+ * One-time per-device setup for the current device: kernel attributes such
+ * as the dynamic shared-memory limit, the side stream and its events, and
+ * the loading of the module that holds verify_attn_run_static's 32 MiB
+ * array (which commits that memory).  Every entry point calls it lazily,
+ * but callers that capture CUDA graphs should call it once before
+ * capturing, and callers that reserve most of the GPU's memory should call
+ * it before reserving.  Returns VA_OK, VA_ERR_DEVICE or VA_ERR_LAUNCH.
  */
 VERIFY_ATTN_API int verify_attn_init(void);
 
@@ -234,15 +237,26 @@ VERIFY_ATTN_API int verify_attn_run_profiled(int impl, void *const *events,
  * VA_ERR_SCRATCH_LIMIT before anything is launched.  The call allocates
  * nothing (no cudaMalloc, no cudaFree, no allocating library routine).
  *
- * The first call on each device looks up the array's device address with
- * that device current and caches it; make that first call before any stream
- * capture.  All calls on a device share the one array and it keeps the last
+ * Set-up: the array's memory is committed on a device when the library's
+ * module holding it loads there, which verify_attn_init() forces.  Call
+ * verify_attn_init() on each device at start-up, before reserving the rest
+ * of its memory and before any stream capture; otherwise the first call of
+ * any entry point does it (and could then fail with VA_ERR_LAUNCH for lack
+ * of memory).  Each call looks the array's device address up again, so no
+ * address is cached across calls.
+ *
+ * Sharing: all calls on a device use the one array and it keeps the last
  * call's contents; each call clears the part that must start at zero (the
  * status word).  Calls whose GPU work overlaps -- for instance on two
- * streams at once -- race on that array, so serialise them.  The status
- * word lives inside the array and is not readable by the caller.
+ * streams at once -- race on that array, so serialise them.  The status word
+ * of the last call is readable through verify_attn_static_status_word().
  *
- * Arguments, layouts and the other return codes are those of verify_attn_run.
+ * The library's per-device state (this array's module, the side stream and
+ * events, the tensor-map cache) belongs to the device's primary context:
+ * after cudaDeviceReset, or under another context, it is not valid.
+ *
+ * Arguments, layouts and the other return codes are those of
+ * verify_attn_run (a device that is not sm_103 gives VA_ERR_DEVICE).
  */
 VERIFY_ATTN_API int verify_attn_run_static(const void *q, int64_t q_stride_tok, int64_t q_stride_head,
                                            const void *kv_pool, int64_t pool_size,
@@ -253,6 +267,20 @@ VERIFY_ATTN_API int verify_attn_run_static(const void *q, int64_t q_stride_tok, 
                                            void *out, int64_t out_stride_tok, int64_t out_stride_head,
                                            int batch, int max_q_per_req, int num_heads, int num_splits,
                                            verify_attn_stream_t stream);
+
+/*
+ * Device address of the status word that verify_attn_run_static calls on
+ * the current device write (bits VA_STATUS_*, as at workspace byte 0 of
+ * verify_attn_run): after its own synchronisation a caller of
+ * verify_attn_run_static reads the 32-bit word there (for instance with
+ * cudaMemcpy to a host variable) to learn of bad slots, bad metadata or a
+ * timed-out wait in the last call.  The pointer is device memory of the
+ * library's static array; it stays valid until the process exits (see the
+ * context note above).  Allocates nothing.  Returns VA_OK, VA_ERR_NULL
+ * (status is null), VA_ERR_DEVICE or VA_ERR_LAUNCH.  (The pages have no
+ * counterpart.)
+ */
+VERIFY_ATTN_API int verify_attn_static_status_word(unsigned int **status);
 
 /*
  * KV save of the draft tokens ("The Launch Wrapper", section The KV Cache
@@ -301,6 +329,33 @@ VERIFY_ATTN_API int verify_attn_save_and_run(const void *kv_new, int64_t kv_new_
                                              int batch, int max_q_per_req, int num_heads, int num_splits,
                                              void *workspace, size_t workspace_bytes,
                                              verify_attn_stream_t stream);
+
+/* Bounds of verify_attn_check_wait_timeout's limit: 1 us to 1 s. */
+#define VERIFY_ATTN_WAIT_PROBE_MIN_NS 1000ull
+#define VERIFY_ATTN_WAIT_PROBE_MAX_NS 1000000000ull
+
+/*
+ * Self-test of the kernels' failure path ("The Launch Wrapper", section The
+ * Design Decision: Three Modes of Operation: a failed kernel must leave the
+ * service able to fall back).  Every wait inside the split kernels is
+ * bounded: when it expires the kernel sets VA_STATUS_TIMEOUT, unwinds and
+ * returns instead of hanging the GPU.  This call launches one small kernel
+ * whose single warp runs that same bounded wait on a barrier nothing ever
+ * arrives on, with a limit of limit_ns nanoseconds (the split kernels use
+ * 1 s), so the expiry path runs on demand.  On `stream`: clears the status
+ * word at workspace byte 0, then the kernel sets VA_STATUS_TIMEOUT in it
+ * and returns after about limit_ns; the caller reads the word after its own
+ * synchronisation, and the context stays usable for normal calls.
+ *
+ *   workspace   at least 256 bytes, 256-B aligned (device memory).
+ *   limit_ns    in [VERIFY_ATTN_WAIT_PROBE_MIN_NS, VERIFY_ATTN_WAIT_PROBE_MAX_NS].
+ *
+ * Allocates nothing, does not synchronise.  Returns VA_OK, VA_ERR_NULL,
+ * VA_ERR_ALIGN, VA_ERR_WORKSPACE, VA_ERR_DIMS (limit out of bounds),
+ * VA_ERR_DEVICE or VA_ERR_LAUNCH.
+ */
+VERIFY_ATTN_API int verify_attn_check_wait_timeout(uint64_t limit_ns, void *workspace, size_t workspace_bytes,
+                                                   verify_attn_stream_t stream);
 
 /* Short English description of a VA_* status code (static storage). */
 VERIFY_ATTN_API const char *verify_attn_status_string(int status);

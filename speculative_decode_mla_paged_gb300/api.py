@@ -64,6 +64,8 @@ def load_library():
             lib.verify_attn_save_kv.restype = _i32
             lib.verify_attn_save_and_run.argtypes = [_p, _i64] + _RUN_ARGS
             lib.verify_attn_save_and_run.restype = _i32
+            lib.verify_attn_check_wait_timeout.argtypes = [ctypes.c_uint64, _p, ctypes.c_size_t, _p]
+            lib.verify_attn_check_wait_timeout.restype = _i32
             lib.verify_attn_status_string.argtypes = [_i32]
             lib.verify_attn_status_string.restype = ctypes.c_char_p
             _lib = lib
@@ -196,6 +198,20 @@ def save_kv(kv_new: torch.Tensor, out_cache_loc: torch.Tensor, kv_pool: torch.Te
                                  ctypes.c_void_p(s.cuda_stream))
     if rc != 0:
         raise VerifyAttnError(f"verify_attn_save_kv: {status_string(rc)} ({rc})")
+
+
+def check_wait_timeout(limit_ns: int, workspace: torch.Tensor, stream: Optional[torch.cuda.Stream] = None) -> None:
+    """Launch the failure-path self-test (verify_attn_check_wait_timeout):
+    one warp runs the split kernels' bounded wait on a barrier nothing
+    arrives on, gives up after ``limit_ns`` and sets STATUS_TIMEOUT in the
+    status word of ``workspace`` (a uint8 CUDA tensor of at least 256
+    bytes; read it with ``read_status`` after the stream's work is done)."""
+    _check_dev("workspace", workspace, torch.uint8)
+    s = stream if stream is not None else torch.cuda.current_stream(workspace.device)
+    rc = load_library().verify_attn_check_wait_timeout(int(limit_ns), _ptr(workspace), workspace.numel(),
+                                                        ctypes.c_void_p(s.cuda_stream))
+    if rc != 0:
+        raise VerifyAttnError(f"verify_attn_check_wait_timeout: {status_string(rc)} ({rc})")
 
 
 def read_status(workspace: torch.Tensor) -> int:

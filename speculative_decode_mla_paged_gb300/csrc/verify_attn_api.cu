@@ -20,6 +20,8 @@ namespace va {
 cudaError_t tc_init();
 cudaError_t launch_tc_split(const Params &p, cudaStream_t stream);
 bool tc_supported(const Params &p);
+int static_scratch_setup();   // verify_attn_static.cu
+cudaError_t launch_wait_probe(unsigned *status, uint64_t limit_ns, cudaStream_t stream);
 
 namespace {
 
@@ -38,6 +40,9 @@ int ensure_init()
     if (major != 10 || minor != 3) return VA_ERR_DEVICE;   // built for sm_103a only
     if (simt_init() != cudaSuccess) return VA_ERR_LAUNCH;
     if (tc_init() != cudaSuccess) return VA_ERR_LAUNCH;
+    // The static-scratch entry point's array: its memory is committed now,
+    // while the caller can still make room, not at that entry point's first call.
+    if (static_scratch_setup() != VA_OK) return VA_ERR_LAUNCH;
     g_init_mask.fetch_or(bit, std::memory_order_acq_rel);
     return VA_OK;
 }
@@ -255,6 +260,22 @@ int verify_attn_save_and_run(const void *kv_new, int64_t kv_new_stride_tok, cons
                    kv_indices, out_cache_loc, custom_mask, mask_indptr, sm_scale, out, out_stride_tok,
                    out_stride_head, batch, max_q_per_req, num_heads, num_splits, workspace, workspace_bytes,
                    stream, nullptr, &save);
+}
+
+int verify_attn_check_wait_timeout(uint64_t limit_ns, void *workspace, size_t workspace_bytes,
+                                   verify_attn_stream_t stream)
+{
+    if (workspace == nullptr) return VA_ERR_NULL;
+    if (!va::aligned(workspace, 256)) return VA_ERR_ALIGN;
+    if (workspace_bytes < va::WS_HEADER) return VA_ERR_WORKSPACE;
+    if (limit_ns < VERIFY_ATTN_WAIT_PROBE_MIN_NS || limit_ns > VERIFY_ATTN_WAIT_PROBE_MAX_NS) return VA_ERR_DIMS;
+    const int rc = va::ensure_init();
+    if (rc != VA_OK) return rc;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    unsigned *status = static_cast<unsigned *>(workspace);
+    if (cudaMemsetAsync(status, 0, sizeof(unsigned), s) != cudaSuccess) return VA_ERR_LAUNCH;
+    if (va::launch_wait_probe(status, limit_ns, s) != cudaSuccess) return VA_ERR_LAUNCH;
+    return VA_OK;
 }
 
 const char *verify_attn_status_string(int status)

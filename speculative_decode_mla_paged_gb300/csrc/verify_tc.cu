@@ -172,14 +172,14 @@ __device__ __forceinline__ int64_t tile_key0(const Unit &u, int t)
 // ------------------------------------------------------------------ bounded waits
 
 __device__ __forceinline__ bool wait_slow(Header *h, uint32_t bar, uint32_t parity, unsigned *status, bool cluster,
-                                       bool stop_on_abort)
+                                       bool stop_on_abort, uint64_t limit_ns)
 {
     const uint64_t t0 = globaltimer_ns();
     for (uint32_t it = 1;; ++it) {
         if (cluster ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity)) return true;
         if ((it & 63u) == 0) {
             if (stop_on_abort && *reinterpret_cast<volatile uint32_t *>(&h->abort)) return false;
-            if (globaltimer_ns() - t0 > TIMEOUT_NS) {
+            if (globaltimer_ns() - t0 > limit_ns) {
                 if (stop_on_abort) {
                     atomicOr(status, STATUS_TIMEOUT);
                     *reinterpret_cast<volatile uint32_t *>(&h->abort) = 1u;
@@ -193,18 +193,36 @@ __device__ __forceinline__ bool wait_slow(Header *h, uint32_t bar, uint32_t pari
 // Wait for phase `parity` of a barrier.  False after a timeout (status bit
 // set, abort flag raised) or when another thread of the CTA aborted.
 __device__ __forceinline__ bool wait_bar(Header *h, uint32_t bar, uint32_t parity, unsigned *status,
-                                         bool cluster = false, bool stop_on_abort = true)
+                                         bool cluster = false, bool stop_on_abort = true,
+                                         uint64_t limit_ns = TIMEOUT_NS)
 {
     if (cluster ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity)) return true;
-    return wait_slow(h, bar, parity, status, cluster, stop_on_abort);
+    return wait_slow(h, bar, parity, status, cluster, stop_on_abort, limit_ns);
 }
 
 // The same for all 32 lanes of a warp (keeps the warp converged for the
 // .sync.aligned tcgen05 instructions that follow).
 __device__ __forceinline__ bool warp_wait(Header *h, uint32_t bar, uint32_t parity, unsigned *status,
-                                          bool cluster = false)
+                                          bool cluster = false, uint64_t limit_ns = TIMEOUT_NS)
 {
-    return __all_sync(0xffffffffu, wait_bar(h, bar, parity, status, cluster)) != 0;
+    return __all_sync(0xffffffffu, wait_bar(h, bar, parity, status, cluster, true, limit_ns)) != 0;
+}
+
+// Self-test of the failure path: one warp waits, with the split kernel's
+// own bounded wait, on an mbarrier that nothing ever arrives on.  The wait
+// must give up after `limit_ns`, set STATUS_TIMEOUT and the abort flag, and
+// the kernel must return, leaving the context usable.
+__global__ void __launch_bounds__(32, 1) wait_probe_kernel(unsigned *status, uint64_t limit_ns)
+{
+    __shared__ __align__(16) Header hs;
+    Header *h = &hs;
+    if (threadIdx.x == 0) {
+        mbar_init(smem_u32(&h->drain), 1);
+        h->abort = 0u;
+    }
+    __syncthreads();
+    if (warp_wait(h, smem_u32(&h->drain), 0u, status, false, limit_ns))
+        atomicOr(status, 0x80000000u);   // cannot happen: nothing arrives; a set top bit would show it did
 }
 
 // After a timeout: TMA gathers and bulk copies already issued into this
@@ -1042,6 +1060,12 @@ cudaError_t tc_init()
 }
 
 bool tc_supported(const Params &p) { return p.pool_size < ((int64_t)1 << 31); }
+
+cudaError_t launch_wait_probe(unsigned *status, uint64_t limit_ns, cudaStream_t stream)
+{
+    wait_probe_kernel<<<1, 32, 0, stream>>>(status, limit_ns);
+    return cudaGetLastError();
+}
 
 namespace {
 
