@@ -1,5 +1,4 @@
 """GPU parity: the CUDA path (through the C ABI) against the CPU oracle."""
-import copy
 
 import numpy as np
 import pytest
@@ -387,41 +386,6 @@ def test_concurrent_mixed_calls_from_two_threads():
         t.join()
     assert not errors, errors
 
-
-@pytest.mark.parametrize("name", ["ragged", "long"])
-def test_bench_launch_configuration_sampled_rows(name):
-    """The configurations bench.py chooses among: the full-size workload at
-    each of the split counts it times (the grid simulation's four best), one
-    call captured in a CUDA graph and replayed after an L2 flush; sampled
-    rows (first and last of every request plus random ones) against the
-    oracle after each of two replays."""
-    from speculative_decode_mla_paged_gb300 import tuning
-
-    inp = W.make_config_inputs(name, device="cuda")
-    d = device_inputs(inp)
-    host = copy.copy(inp)
-    host.q, host.kv_pool = inp.q.cpu(), inp.kv_pool.cpu()
-    rows = sample_rows(host, n_random=32, seed=11)
-    ref = oracle_rows(host, rows)
-    flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
-    for splits in tuning.ranked_num_splits(inp.prefix_lens, inp.draft_lens, inp.num_heads, k=4):
-        runner = api.VerifyAttention(inp.batch, inp.max_q_per_req, inp.num_heads, splits)
-        out = torch.zeros(inp.total_q, inp.num_heads, 512, dtype=torch.bfloat16, device="cuda")
-        g = torch.cuda.CUDAGraph()
-        s = torch.cuda.Stream()
-        torch.cuda.synchronize()
-        with torch.cuda.stream(s):
-            with torch.cuda.graph(g, stream=s):
-                runner(d["q"], d["kv_pool"], d["qo_indptr"], d["kv_indptr"], d["kv_indices"], d["out_cache_loc"],
-                       d["custom_mask"], d["mask_indptr"], inp.sm_scale, out)
-        for _ in range(2):
-            out.zero_()
-            flush.zero_()
-            g.replay()
-            torch.cuda.synchronize()
-            assert runner.status() == 0
-            assert_parity(as_rows(out)[rows], ref, f"{name}/graph/{splits} splits")
-        del g, runner
 
 def test_tune_num_splits_returns_a_candidate_and_a_correct_call():
     """api.tune_num_splits times each candidate as graph replays of the real
