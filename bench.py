@@ -27,6 +27,7 @@ other ranks exit 0 at once).
 from __future__ import annotations
 
 import argparse
+import copy
 import hashlib
 import json
 import os
@@ -62,7 +63,9 @@ def parse_args():
     ap.add_argument("--kernel", choices=["tc", "simt"], default="tc")
     ap.add_argument("--num-splits", type=int, default=0, help="0 = per-config default")
     ap.add_argument("--no-per-config", action="store_true", help="skip the five-config table")
-    ap.add_argument("--cpu-seconds", type=float, default=12.0, help="oracle sample budget")
+    ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle timings")
+    ap.add_argument("--cpu-seconds", type=float, default=None,
+                    help="accepted for older profile commands; the oracle is now timed on whole calls")
     ap.add_argument("--launch-only", action="store_true",
                     help="for profilers: W warm-up and K timed direct calls of the workload, nothing else")
     return ap.parse_args()
@@ -278,41 +281,113 @@ def time_oracle(inp, seconds, seed=0):
                          "pairs": int(pairs), "of_pairs": int(total_pairs)}
 
 
+def cpu_model() -> str:
+    """The host CPU's model name (x86: /proc/cpuinfo; Arm: lscpu), or '' if unknown."""
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if line.lower().startswith("model name"):
+                    return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.strip().lower().startswith("model name"):
+                return line.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    import platform
+    return platform.processor() or platform.machine()
+
+
+def time_oracle_call(inp, threads=None):
+    """Wall seconds of one whole oracle call (every output row) on `threads`
+    host threads (None: all of them)."""
+    import oracle
+    cores = oracle.num_threads()
+    if threads is not None:
+        oracle.set_num_threads(threads)
+    try:
+        t0 = time.perf_counter()
+        oracle.run(inp)
+        return time.perf_counter() - t0
+    finally:
+        if threads is not None:
+            oracle.set_num_threads(cores)
+
+
+def oracle_timings(inp, single_core_budget_s=20.0):
+    """The oracle on this host for one workload: a whole call on all cores,
+    and on one core either a whole call (when the all-core time x cores
+    predicts at most `single_core_budget_s`) or a row sample of about 4 s
+    scaled to a full call by visible (row, key) pairs, labelled as such."""
+    import oracle
+    cores = oracle.num_threads()
+    all_s = time_oracle_call(inp)
+    rec = {"all_cores_s": all_s, "cores": cores, "rows": int(inp.total_q * inp.num_heads)}
+    if all_s * cores <= single_core_budget_s:
+        rec["single_core_s"] = time_oracle_call(inp, threads=1)
+        rec["single_core_how"] = "whole call"
+    else:
+        oracle.set_num_threads(1)
+        try:
+            us, sample = time_oracle(inp, 4.0, seed=1)
+        finally:
+            oracle.set_num_threads(cores)
+        rec["single_core_s"] = us / 1e6
+        rec["single_core_how"] = (f"row sample: {sample['rows']} of {sample['of_rows']} rows in "
+                                  f"{sample['seconds']} s, scaled by visible (row, key) pairs")
+    return rec
+
+
+def reference_inputs(config):
+    """The workload's inputs on the host (large pools are drawn on the GPU
+    when one is present, as our arm draws them, then copied)."""
+    from speculative_decode_mla_paged_gb300 import workloads as W
+    if config in ("tiny", "short"):
+        return W.make_config_inputs(config, device="cpu")
+    import torch
+    if torch.cuda.is_available():
+        inp = W.make_config_inputs(config, device="cuda")
+        inp.q, inp.kv_pool = inp.q.cpu(), inp.kv_pool.cpu()
+        torch.cuda.empty_cache()
+        return inp
+    return W.make_config_inputs(config, device="cpu")
+
+
+REFERENCE_BUDGET_S = 150.0
+
+
 def run_reference(args):
-    """The oracle, as it stands, on the host cores: K timed steps of a bounded sample."""
+    """The oracle, as it stands, on the host cores: whole calls of the
+    workload (every output row), as many of the requested W + K as fit in
+    about REFERENCE_BUDGET_S; the line reports the counts actually run."""
     world, rank, _ = dist_setup(args)
     if rank != 0:
         return
     import oracle
     from speculative_decode_mla_paged_gb300 import workloads as W
     oracle.build()
-    inp = W.make_config_inputs(args.config, device="cpu") if args.config in ("tiny", "short") else None
-    if inp is None:
-        import torch
-        if torch.cuda.is_available():
-            inp = W.make_config_inputs(args.config, device="cuda")
-            inp.q, inp.kv_pool = inp.q.cpu(), inp.kv_pool.cpu()
-        else:
-            inp = W.make_config_inputs(args.config, device="cpu")
-    per_step = max(2.0, min(20.0, 150.0 / max(1, args.steps + args.warmup)))
-    for w in range(args.warmup):
-        time_oracle(inp, per_step / 4, seed=1000 + w)
-    vals, samples = [], []
-    for k in range(args.steps):
-        v, s = time_oracle(inp, per_step, seed=k)
-        vals.append(v); samples.append(s)
-    value = statistics.mean(vals)
+    inp = reference_inputs(args.config)
+    t_begin = time.perf_counter()
+    warm = [time_oracle_call(inp)]          # one untimed whole call, which also sizes the run
+    per_call = warm[0]
+    left = REFERENCE_BUDGET_S - (time.perf_counter() - t_begin)
+    steps = max(1, min(args.steps, int(left // max(per_call, 1e-6))))
+    vals = [time_oracle_call(inp) for _ in range(steps)]
+    value = statistics.mean(vals) * 1e6
     cores = oracle.num_threads()
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
-        "steps": args.steps, "warmup": args.warmup, "ms_per_step": value / 1e3,
-        "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-        "data": "synthetic", "config": {"workload": f"{args.config}: {W.CONFIGS[args.config].description}",
-                                        "name": args.config},
-        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
-                         "sample": f"per step {samples[0]['rows']} of {samples[0]['of_rows']} output rows "
-                                   f"({statistics.mean(s['seconds'] for s in samples):.2f} s, budget "
-                                   f"{per_step:.0f} s), scaled to a full call by visible (row, key) pairs"},
+        "steps": steps, "warmup": len(warm), "steps_requested": args.steps, "warmup_requested": args.warmup,
+        "ms_per_step": value / 1e3, "higher_is_better": False, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f64", "data": "synthetic",
+        "config": {"workload": f"{args.config}: {W.CONFIGS[args.config].description}", "name": args.config},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle", "cpu_model": cpu_model(),
+                         "sample": f"whole calls (all {inp.total_q * inp.num_heads} output rows): {len(warm)} "
+                                   f"untimed, then {steps} timed, of the {args.warmup} + {args.steps} requested "
+                                   f"(whole calls bounded to about {REFERENCE_BUDGET_S:.0f} s)"},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -568,7 +643,11 @@ def run_ours(args):
 
     # ---- the five workloads and the two extra ones (chain verify, decode),
     # device time per call (informational)
-    if rank == 0 and not args.no_per_config:
+    headline_oracle = None
+    if not args.no_cpu:
+        import oracle
+        oracle.build()
+    if not args.no_per_config:
         table = {}
         for name in W.CONFIG_ORDER + W.EXTRA_CONFIG_ORDER:
             ci = inp if name == args.config else W.make_config_inputs(name, device=dev)
@@ -583,29 +662,32 @@ def run_ours(args):
                            "tflops": f / tc / 1e12, "kv_gbs": b / tc / 1e9,
                            "roofline_frac": max(f / (peaks["bf16_tflops"] * 1e12),
                                                 b / (peaks["hbm_gbs"] * 1e9)) / tc,
-                           "num_splits": cs}
+                           "num_splits": cs, "timing": "direct calls, L2 flushed, 3 warm-up + 5 timed"}
+            if not args.no_cpu:
+                host = ci if name != args.config else copy.copy(ci)
+                host.q, host.kv_pool = ci.q.cpu(), ci.kv_pool.cpu()
+                table[name]["cpu_oracle"] = oracle_timings(host)
+                if name == args.config:
+                    headline_oracle = table[name]["cpu_oracle"]
+                del host
             if name != args.config:
                 del cd, cr, ci
                 torch.cuda.empty_cache()
         line["per_config"] = table
 
-    # ---- CPU oracle baseline on the host cores (rank 0, N = 1 only)
-    if rank == 0 and world == 1:
-        import oracle
-        oracle.build()
-        inp.q, inp.kv_pool = inp.q.cpu(), inp.kv_pool.cpu()
-        us, sample = time_oracle(inp, args.cpu_seconds)
-        cores = oracle.num_threads()
-        line["cpu_baseline"] = {"value": us, "unit": UNIT, "cores": cores, "kind": "oracle",
-                                "sample": f"{sample['rows']} of {sample['of_rows']} output rows "
-                                          f"({sample['seconds']} s), scaled to a full call by visible "
-                                          "(row, key) pairs"}
-        oracle.set_num_threads(1)
-        us1, sample1 = time_oracle(inp, min(3.0, args.cpu_seconds / 4), seed=1)
-        oracle.set_num_threads(cores)
-        line["cpu_baseline"]["single_core"] = {
-            "value": us1, "unit": UNIT, "cores": 1,
-            "sample": f"{sample1['rows']} output rows ({sample1['seconds']} s), scaled the same way"}
+    # ---- CPU oracle baseline on the host cores: one whole call of the
+    # headline workload on all cores (and on one core, see oracle_timings)
+    if not args.no_cpu:
+        if headline_oracle is None:
+            host = copy.copy(inp)
+            host.q, host.kv_pool = inp.q.cpu(), inp.kv_pool.cpu()
+            headline_oracle = oracle_timings(host)
+        line["cpu_baseline"] = {
+            "value": headline_oracle["all_cores_s"] * 1e6, "unit": UNIT, "cores": headline_oracle["cores"],
+            "kind": "oracle", "cpu_model": cpu_model(),
+            "sample": f"one whole call (all {headline_oracle['rows']} output rows), timed, not scaled",
+            "single_core": {"value": headline_oracle["single_core_s"] * 1e6, "unit": UNIT, "cores": 1,
+                            "sample": headline_oracle["single_core_how"]}}
     print(json.dumps(line), flush=True)
 
 
