@@ -142,6 +142,45 @@ def profiled_traffic(kernel, cfg_name):
     return None
 
 
+# Issued tensor-core work per MMA instruction of the tensor-core kernel: every
+# 128-key tile of 128 rows takes 36 score MMAs (M128 N128 K16) and 16 P V
+# MMAs (M128 N256 K16), always in that ratio, so FLOPs per instruction
+# average out to this over any whole number of tiles.
+TC_FLOP_PER_MMA_INST = (36 * 2 * 128 * 128 * 16 + 16 * 2 * 128 * 256 * 16) / 52
+
+
+def profiled_tensor_pipe(kernel, cfg_name):
+    """Tensor-pipe counters of the split phase of one call (all its split
+    launches) from a committed ncu summary for this exact kernel source:
+    {"active_cycles": sm__pipe_tensor_cycles_active.sum, "units": the number
+    of instances that sum runs over, "mma_inst": sm__inst_executed_pipe_tensor.sum},
+    or None."""
+    path = os.path.join(ROOT, "profiles", "tensor_pipe.md")
+    if not os.path.exists(path):
+        return None
+    h = kernel_hash(kernel)
+    num = r"\s*([0-9.e+]+)\s*\|"
+    for line in open(path):
+        m = re.match(r"\|\s*(\w+)\s*\|\s*(\w+)\s*\|\s*([0-9a-f]{12})\s*\|" + num * 3, line)
+        if m and m.group(1) == kernel and m.group(2) == cfg_name and m.group(3) == h:
+            return {"active_cycles": float(m.group(4)), "units": float(m.group(5)), "mma_inst": float(m.group(6))}
+    return None
+
+
+def tensor_pipe_summary(counters, split_s, sm_mhz, flops):
+    """What the counters say about the timed split phase: the share of the
+    tensor pipes' cycles in which they were active (counter cycles over
+    instances x split-phase time x the sampled SM clock), the issued MMA FLOPs
+    and their ratio to the algorithmic FLOPs (the padding of partial and
+    masked tiles and of rows past a request's end)."""
+    if counters is None or not split_s or not sm_mhz:
+        return None
+    issued = counters["mma_inst"] * TC_FLOP_PER_MMA_INST
+    return {"active_frac": counters["active_cycles"] / (counters["units"] * split_s * sm_mhz * 1e6),
+            "issued_flops": issued, "issued_over_algorithmic": issued / flops,
+            "source": "profiles/tensor_pipe.md (ncu, same kernel source)"}
+
+
 class ClockSampler:
     """nvidia-smi clocks / throttle reasons sampled every 200 ms during the timed region."""
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
@@ -611,6 +650,8 @@ def run_ours(args):
         roof = {"bound": "hbm", "achieved": nbytes / split_s / 1e9, "peak": peaks["hbm_gbs"], "unit": "GB/s"}
     roof["frac"] = roof["achieved"] / roof["peak"]
     roof["traffic"] = profiled_traffic(args.kernel, args.config)
+    roof["tensor_pipe"] = tensor_pipe_summary(profiled_tensor_pipe(args.kernel, args.config), split_s,
+                                              (clocks or {}).get("sm_mhz"), flops)
     roof["peak_source"] = f"{peak_src} (burst; kernel timed alone)"
     roof["kernel"] = (f"{args.kernel} split phase (the split launches of one call, concurrent when both "
                       "tensor-core cluster shapes run; traffic summed over them)")
@@ -655,14 +696,18 @@ def run_ours(args):
             cs = splits if name == args.config else (args.num_splits or choose_splits(ci, cd, args.kernel)[0])
             cr = runner if name == args.config else api.VerifyAttention(ci.batch, ci.max_q_per_req,
                                                                           ci.num_heads, cs, impl=args.kernel)
+            gm, gs, _, _ = measure_graph(ci, cd, cr, 10, 3, flush, torch)
             cm, sm, _ = measure(ci, cd, cr, 5, 3, flush, torch)
             f, b = ci.algorithmic_flops(), ci.algorithmic_bytes()
-            tc = statistics.mean(cm) / 1e3
-            table[name] = {"us_per_call": tc * 1e6, "split_us": statistics.mean(sm) * 1e3,
-                           "tflops": f / tc / 1e12, "kv_gbs": b / tc / 1e9,
-                           "roofline_frac": max(f / (peaks["bf16_tflops"] * 1e12),
-                                                b / (peaks["hbm_gbs"] * 1e9)) / tc,
-                           "num_splits": cs, "timing": "direct calls, L2 flushed, 3 warm-up + 5 timed"}
+            tg, tgs = statistics.mean(gm) / 1e3, statistics.mean(gs) / 1e3
+            t_roof = max(f / (peaks["bf16_tflops"] * 1e12), b / (peaks["hbm_gbs"] * 1e9))
+            table[name] = {"us_per_call": tg * 1e6, "split_us": tgs * 1e6,
+                           "tflops": f / tg / 1e12, "kv_gbs": b / tg / 1e9,
+                           "roofline_frac": t_roof / tg, "roofline_frac_split": t_roof / tgs,
+                           "num_splits": cs,
+                           "timing": "cold CUDA-graph replays (L2 flushed), 3 warm-up + 10 timed",
+                           "direct_us_per_call": statistics.mean(cm) * 1e3,
+                           "direct_split_us": statistics.mean(sm) * 1e3}
             if not args.no_cpu:
                 host = ci if name != args.config else copy.copy(ci)
                 host.q, host.kv_pool = ci.q.cpu(), ci.kv_pool.cpu()
