@@ -44,10 +44,15 @@
 // softmax / row warpgroups.
 //
 // Online softmax with a lazy maximum: O is rescaled only when a row's
-// running maximum grows by more than 2^8 (log2 units), so P stays <= 256.
-// The P transfer of a tile's first half carries the per-row factor and a
-// per-warp flag; the O CTA's row warps rescale their TMEM rows only when a
-// flag is set.
+// running maximum grows by more than 32 (log2 units), so P stays <= 2^32.
+// A rescale drains the P V MMAs and round-trips O through registers, so it
+// is kept rare; the bound is set by range, not precision: P is bf16 (8
+// exponent bits, like fp32), rounding is relative and so independent of the
+// scale, and the fp32 sums l <= n 2^32 and |O| <= n 2^32 max|v| stay finite
+// for any n < 2^31 keys and |v| < 2^64.  A row's first visible key needs no
+// rescale (its O and l are still exactly 0).  The P transfer of a tile's
+// first half carries the per-row factor and a per-warp flag; the O CTA's
+// row warps rescale their TMEM rows only when a flag is set.
 //
 // Synchronisation uses mbarriers only: TMA and bulk-copy bytes complete
 // barriers directly, tensor-core commits arrive on them (across the pair
@@ -81,6 +86,8 @@ constexpr int REGS_WIDE = 128;             // softmax and O-row warpgroups after
 constexpr int REGS_NARROW = 48;            // producer, MMA and idle warpgroups
 static_assert(8 * 32 * REGS_WIDE + 20 * 32 * REGS_NARROW <= THREADS * LAUNCH_REGS,
               "the register split fits the launch allocation");
+static_assert(4 * 32 * REGS_WIDE + 24 * 32 * REGS_NARROW <= THREADS * LAUNCH_REGS,
+              "the O CTA's split fits the launch allocation");
 constexpr uint32_t K_CHUNKS = D / 64;      // 9 column chunks per S tile
 constexpr uint32_t KCHUNK = KEYS_S * 128;  // 16 KB: 128 keys x 64 dims
 constexpr int RCHUNKS = 3;                 // S: chunks per gather round
@@ -124,7 +131,7 @@ constexpr uint32_t IDESC_S = idesc_bf16(128, 128, false);
 constexpr uint32_t IDESC_PV = idesc_bf16(128, 256, true);
 constexpr float LOG2E = 1.4426950408889634f;
 constexpr float LN2 = 0.69314718055994531f;
-constexpr float RESCALE_LOG2 = 8.0f;
+constexpr float RESCALE_LOG2 = 32.0f;         // lazy-rescale threshold (log2 units)
 constexpr uint64_t TIMEOUT_NS = 1000000000ull;
 
 // Shared-memory header at the (1 KB aligned) base; same offsets in both CTAs
@@ -394,9 +401,26 @@ __device__ void s_gather(const Params &p, Header *h, const CUtensorMap *tmap, co
 //
 // S[buf] = Q K^T round by round: 32 MMAs with Q's no-PE dims from TMEM, then
 // 4 with Q's RoPE dims from shared memory; each round is released by a commit.
+//
+// One thread issues every MMA, so its instruction stream sets the MMA rate:
+// an M = 128, N = 128, K = 16 MMA occupies the tensor pipe for 64 cycles, and
+// building a descriptor from an address costs about as much again in
+// dependent integer operations.  So the descriptors are built once, before
+// the loops, and advanced by constants: the start address sits in the low 14
+// bits in 16-B units, and shared-memory offsets below 256 KB never carry out
+// of it, so desc(addr + off) = desc(addr) + off / 16.
+static_assert(SMEM_ALLOC < (256u << 10), "descriptor arithmetic needs shared-memory offsets below 256 KB");
+
+__device__ __forceinline__ uint64_t desc_add(uint64_t desc, uint32_t byte_off)
+{
+    return desc + (uint64_t)(byte_off >> 4);
+}
+
 template <int NT>
 __device__ void s_mma(const Params &p, Header *h, uint32_t smem, uint32_t tmem, const Unit &u)
 {
+    const uint64_t ring_desc = sdesc_sw128(smem + S_RING, 16u, 1024u);
+    const uint64_t qpe_desc = sdesc_sw128(smem + S_QPE, 16u, 1024u);
     for (int t = 0; t < u.ntiles; ++t) {
         const int buf = t & 1;
         if (t >= 2 && !wait_bar(h, smem_u32(&h->s_free[buf]), (uint32_t)((t >> 1) - 1) & 1u, p.status)) break;
@@ -423,18 +447,16 @@ __device__ void s_mma(const Params &p, Header *h, uint32_t smem, uint32_t tmem, 
 #pragma unroll
             for (int cc = 0; cc < RCHUNKS; ++cc) {
                 const int c = g * RCHUNKS + cc;
-                const uint32_t sb = smem + S_RING + (uint32_t)g * KROUND + (uint32_t)cc * KCHUNK;
+                const uint64_t b = desc_add(ring_desc, (uint32_t)g * KROUND + (uint32_t)cc * KCHUNK);
                 if (c < 8) {
-                    const uint32_t a = tmem + 32u * (uint32_t)c;
 #pragma unroll
                     for (int k = 0; k < 4; ++k)
-                        mma_ts(d, a + 8u * (uint32_t)k, sdesc_sw128(sb + 32u * (uint32_t)k, 16u, 1024u), IDESC_S,
+                        mma_ts(d, tmem + 32u * (uint32_t)c + 8u * (uint32_t)k, desc_add(b, 32u * (uint32_t)k), IDESC_S,
                                (c | k) ? 1u : 0u);
                 } else {
 #pragma unroll
                     for (int k = 0; k < 4; ++k)
-                        mma_ss(d, sdesc_sw128(smem + S_QPE + 32u * (uint32_t)k, 16u, 1024u),
-                               sdesc_sw128(sb + 32u * (uint32_t)k, 16u, 1024u), IDESC_S, 1u);
+                        mma_ss(d, desc_add(qpe_desc, 32u * (uint32_t)k), desc_add(b, 32u * (uint32_t)k), IDESC_S, 1u);
                 }
             }
             mma_commit_multicast(smem_u32(&h->c_empty[g]), Shape<NT>::S_MASK);   // every S CTA may refill the slot
@@ -613,8 +635,10 @@ __device__ void s_softmax(const Params &p, Header *h, uint32_t smem, uint32_t tm
         mx = mx == -INFINITY ? -INFINITY : mx * sl2;   // log2 units
         float alpha = 1.f;
         bool rescale = false;
-        if (mx > m_used + RESCALE_LOG2) {              // also the first tile where the row sees a key
-            alpha = (m_used == -INFINITY) ? 0.f : ex2_approx(m_used - mx);
+        if (m_used == -INFINITY) {
+            m_used = mx;                               // first visible key (or none yet): O and l are 0
+        } else if (mx > m_used + RESCALE_LOG2) {
+            alpha = ex2_approx(m_used - mx);
             l *= alpha;
             m_used = mx;
             rescale = true;
@@ -773,6 +797,8 @@ template <int NT>
 __device__ void o_mma(const Params &p, Header *h, uint32_t smem, uint32_t tmem, const Unit &u)
 {
     const int nt = 2 * u.ntiles;
+    const uint64_t p_desc = sdesc_sw128(smem + O_PSLOT, 16u, 1024u);   // A: P, K-major
+    const uint64_t v_desc = sdesc_sw128(smem + O_VRING, VCHUNK, 1024u);  // B: V, MN-major
     int slot = 0;
     uint32_t phase = 0, nrs = 0;
     uint32_t pphase = 0;       // bit 2g + par: parity of P slot [g][par]'s pending transfer
@@ -781,7 +807,6 @@ __device__ void o_mma(const Params &p, Header *h, uint32_t smem, uint32_t tmem, 
         const int g = ot & 1, par = (ot >> 1) & 1;
         if (!wait_bar(h, smem_u32(&h->p_full[g][par]), (pphase >> (2 * g + par)) & 1u, p.status)) { ok = false; break; }
         pphase ^= 1u << (2 * g + par);
-        const uint32_t pb = smem + O_PSLOT + (uint32_t)(2 * g + par) * PSLOT;
         if (g == 0 && ot > 0) {
             const volatile uint32_t *f = reinterpret_cast<const volatile uint32_t *>(
                 reinterpret_cast<uint8_t *>(h) + O_PSLOT + (2 * g + par) * PSLOT + PTILE + ROWS * 4);
@@ -799,11 +824,12 @@ __device__ void o_mma(const Params &p, Header *h, uint32_t smem, uint32_t tmem, 
         for (int hf = 0; hf < 2; ++hf) {
             if (!wait_bar(h, smem_u32(&h->v_full[slot]), phase, p.status)) { ok = false; break; }
             tc_fence_after_sync();
-            const uint32_t vb = smem + O_VRING + (uint32_t)slot * VHALF;
+            const uint64_t a = desc_add(p_desc, (uint32_t)(2 * g + par) * PSLOT);
+            const uint64_t b = desc_add(v_desc, (uint32_t)slot * VHALF);
 #pragma unroll
             for (int k = 0; k < KEYS_O / 16; ++k)
-                mma_ss(tmem + 256u * (uint32_t)hf, sdesc_sw128(pb + 32u * (uint32_t)k, 16u, 1024u),
-                       sdesc_sw128(vb + (uint32_t)k * 16u * 128u, VCHUNK, 1024u), IDESC_PV, (ot | k) ? 1u : 0u);
+                mma_ss(tmem + 256u * (uint32_t)hf, desc_add(a, 32u * (uint32_t)k), desc_add(b, (uint32_t)k * 16u * 128u),
+                       IDESC_PV, (ot | k) ? 1u : 0u);
             mma_commit_multicast(smem_u32(&h->v_empty[slot]), Shape<NT>::O_MASK);   // every O CTA may refill the slot
             if (++slot == NVH) { slot = 0; phase ^= 1u; }
         }
@@ -976,14 +1002,22 @@ __global__ void __launch_bounds__(THREADS, 1)
     const uint32_t tmem = *reinterpret_cast<volatile uint32_t *>(&h->tmem_base);
 
     // Roles by warpgroup; setmaxnreg moves registers from the producer, MMA
-    // and idle warpgroups to the softmax / row warpgroups.
-    // Every warpgroup returns to the launch budget before the common exit.
+    // and idle warpgroups to the softmax / row warpgroups, once.  No
+    // warpgroup changes its budget again: an increase waits until the pool
+    // covers it, so a narrow warpgroup that handed its registers back and then
+    // asked for them again (an idle one at once, a producer when done) could
+    // take them before a wide warpgroup's increase was served, and in the S
+    // CTA the pool cannot cover both (8 softmax warps at 128, 17 warps at 48
+    // and the MMA warpgroup's 3 idle warps back at 72 need 1280 registers more
+    // than the 896 x 72 launch allocation): a softmax warpgroup would wait
+    // forever.
+    // With decreases only on the narrow side, the one increase per wide
+    // warpgroup is always covered once the decreases have run.
     const bool wide = role == 0 ? warp < PRODUCER_WARP0 : warp < 4;
     if (wide) {
         regs_inc<REGS_WIDE>();
         if (role == 0) s_softmax(p, h, smem, tmem, u);
         else o_rows(p, h, smem, tmem, u);
-        regs_dec<LAUNCH_REGS>();
     } else {
         regs_dec<REGS_NARROW>();
         if (warp >= PRODUCER_WARP0 && warp < MMA_WARP) {
@@ -999,7 +1033,6 @@ __global__ void __launch_bounds__(THREADS, 1)
             }
         }
         __syncwarp();
-        regs_inc<LAUNCH_REGS>();
     }
 
     tc_fence_before_sync();

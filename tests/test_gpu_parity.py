@@ -87,6 +87,40 @@ def test_softmax_scale_and_range(sm_scale, q_scale, impl):
     assert_parity(as_rows(out), oracle_rows(inp), f"{impl}/scale={sm_scale}/q={q_scale}")
 
 
+def _rising_score_inputs(seed):
+    """Scores that climb about 47 (log2 units) every 128 keys: Q's last 64
+    dims are 1 and key j's are 7 j / 128, so the score gains 64 * 7 * scale
+    * log2(e) ~ 47 per 128 keys over a random part of spread ~2.4."""
+    inp = W.make_inputs([1500, 600], [24, 8], 8, 8192, seed=seed)
+    q, pool = inp.q.clone(), inp.kv_pool.clone()
+    q[:, :, 512:] = 1.0
+    for b in range(inp.batch):
+        slots = np.concatenate([inp.kv_indices[inp.kv_indptr[b]:inp.kv_indptr[b + 1]],
+                                inp.out_cache_loc[inp.qo_indptr[b]:inp.qo_indptr[b + 1]]])
+        ramp = torch.tensor(7.0 * np.arange(len(slots)) / 128.0, dtype=torch.float32)
+        pool[torch.from_numpy(slots.astype(np.int64)), 512:] = ramp[:, None].to(torch.bfloat16)
+    inp.q, inp.kv_pool = q, pool
+    return inp
+
+
+@pytest.mark.parametrize("impl", IMPLS)
+@pytest.mark.parametrize("splits", [1, 2])
+def test_rising_scores_rescale_on_every_tile(splits, impl):
+    """Every 128-key window's row maximum exceeds the previous window's by
+    more than 32 (log2 units) in every row, so the tensor-core kernel's lazy
+    maximum must rescale O on every tile: every row against the oracle."""
+    inp = _rising_score_inputs(seed=54)
+    L, T0 = int(inp.prefix_lens[0]), int(inp.draft_lens[0])
+    s = (inp.q[:T0].double().reshape(-1, 576).numpy()
+         @ inp.kv_pool[torch.from_numpy(inp.kv_indices[:L].astype(np.int64))].double().numpy().T)
+    s *= inp.sm_scale * np.log2(np.e)
+    win = s[:, : (L // 128) * 128].reshape(s.shape[0], -1, 128).max(axis=2)
+    assert np.diff(win, axis=1).min() > 32.0, "inputs do not force a rescale per tile"
+    out, status = run(inp, impl=impl, num_splits=splits)
+    assert status == 0
+    assert_parity(as_rows(out), oracle_rows(inp), f"{impl}/rising scores/{splits} splits")
+
+
 def test_large_config_kernels_agree_on_every_row():
     """At full size every row of the tensor-core path matches the CUDA-core
     path within the same bar (the oracle covers the sampled rows above)."""
