@@ -139,7 +139,7 @@ constexpr uint64_t TIMEOUT_NS = 1000000000ull;
 struct Header {
     uint64_t c_full[NKR];      // S: K round landed (8 producer-warp arrives + TMA bytes)
     uint64_t c_empty[NKR];     // S: the MMAs of both S CTAs reading the round completed (2 multicast commits)
-    uint64_t s_full[2];        // S: scores ready (commit) + valid-key bits copied (MMA thread)
+    uint64_t s_full[2];        // S: scores ready (commit) + the MMA thread's arrive (orders the valid bits)
     uint64_t s_free[2];        // S: the 8 softmax warps have read the score buffer
     uint64_t p_empty[2][2];    // S: the partner's P V MMAs on P slot [group][parity] completed (its commit)
     uint64_t v_full[NVH];      // O: V half tile landed (8 producer-warp arrives + TMA bytes)
@@ -150,8 +150,7 @@ struct Header {
     uint64_t rs_done;          // O: the 4 row warps rescaled their rows
     uint64_t l_ready;          // O: the partner's 4 group-0 warps wrote 1/l
     uint64_t drain;            // both: all MMAs of the CTA completed
-    uint16_t t_valid[2][8];    // S: byte w (producer warp w): bit k = key 4w + k, bit 4 + k = key 64 + 4w + k is valid (tile ring of 2)
-    uint64_t s_valid[2][2];    // S: the same bits, per score buffer
+    uint8_t t_valid[4][32];    // S: [tile % 4][key group g]: bit k = key 4g + k of the tile has a valid slot
     uint32_t tmem_base;
     uint32_t abort;
     int32_t rs_slot;           // O: tile parity of the P slot whose factors to apply; -1: finish
@@ -210,9 +209,31 @@ __device__ __forceinline__ bool wait_bar(Header *h, uint32_t bar, uint32_t parit
 // The same for all 32 lanes of a warp (keeps the warp converged for the
 // .sync.aligned tcgen05 instructions that follow).
 __device__ __forceinline__ bool warp_wait(Header *h, uint32_t bar, uint32_t parity, unsigned *status,
-                                          bool cluster = false, uint64_t limit_ns = TIMEOUT_NS)
+                                          bool cluster = false, uint64_t limit_ns = TIMEOUT_NS,
+                                          bool stop_on_abort = true)
 {
-    return __all_sync(0xffffffffu, wait_bar(h, bar, parity, status, cluster, true, limit_ns)) != 0;
+    return __all_sync(0xffffffffu, wait_bar(h, bar, parity, status, cluster, stop_on_abort, limit_ns)) != 0;
+}
+
+// For waits off the critical path (the O row warps, idle until a rescale or
+// the epilogue): the thread sleeps between polls, so it takes no issue
+// slots or ALU cycles from the warps doing the work.  Same bound and abort
+// handling as wait_bar.
+__device__ __forceinline__ bool wait_idle(Header *h, uint32_t bar, uint32_t parity, unsigned *status)
+{
+    const uint64_t t0 = globaltimer_ns();
+    for (uint32_t it = 1;; ++it) {
+        if (mbar_try_wait(bar, parity)) return true;
+        __nanosleep(256);
+        if ((it & 15u) == 0) {
+            if (*reinterpret_cast<volatile uint32_t *>(&h->abort)) return false;
+            if (globaltimer_ns() - t0 > TIMEOUT_NS) {
+                atomicOr(status, STATUS_TIMEOUT);
+                *reinterpret_cast<volatile uint32_t *>(&h->abort) = 1u;
+                return false;
+            }
+        }
+    }
 }
 
 // Self-test of the failure path: one warp waits, with the split kernel's
@@ -346,7 +367,6 @@ __device__ void s_gather(const Params &p, Header *h, const CUtensorMap *tmap, co
     const bool contiguous = unit_contiguous(p, u, pw * 32 + lane);
     bool ok = true;
     for (int t = 0; t < u.ntiles && ok; ++t) {
-        const uint32_t bits8 = __shfl_sync(0xffffffffu, cur.nib, 0) | (__shfl_sync(0xffffffffu, cur.nib, 1) << 4);
         const bool run = contiguous && tile_key0(u, t) + KEYS_S <= u.k1;
         const int base = cur.y[0];                       // warp 0, lane l: the slot of key 64 l
 #pragma unroll 1
@@ -356,8 +376,11 @@ __device__ void s_gather(const Params &p, Header *h, const CUtensorMap *tmap, co
                 break;
             }
             const uint32_t bar = smem_u32(&h->c_full[g]);
+            if (g == 0) {
+                if (act) reinterpret_cast<volatile uint8_t *>(&h->t_valid[t & 3][0])[kg] = (uint8_t)cur.nib;
+                __syncwarp();                                 // lane 1's byte before lane 0's release
+            }
             if (lane == 0) {
-                if (g == 0) reinterpret_cast<volatile uint8_t *>(&h->t_valid[t & 1][0])[pw] = (uint8_t)bits8;
                 if (pw == 0) mbar_arrive_expect_tx(bar, KROUND);   // both halves land here
                 else mbar_arrive(bar);
             }
@@ -397,16 +420,18 @@ __device__ void s_gather(const Params &p, Header *h, const CUtensorMap *tmap, co
     if (!ok) settle_copies();
 }
 
-// ------------------------------------------------------------------ S role: MMA issue (warp 24, lane 0)
+// ------------------------------------------------------------------ S role: MMA issue (warp 24)
 //
 // S[buf] = Q K^T round by round: 32 MMAs with Q's no-PE dims from TMEM, then
 // 4 with Q's RoPE dims from shared memory; each round is released by a commit.
 //
-// One thread issues every MMA, so its instruction stream sets the MMA rate:
-// an M = 128, N = 128, K = 16 MMA occupies the tensor pipe for 64 cycles, and
-// building a descriptor from an address costs about as much again in
-// dependent integer operations.  So the descriptors are built once, before
-// the loops, and advanced by constants: the start address sits in the low 14
+// One lane issues every MMA, and the tensor pipe accepts only a few ahead
+// of the one it runs, so the issuing lane's instruction stream sets the MMA
+// rate: an M = 128, N = 128, K = 16 MMA occupies the pipe for 64 cycles,
+// while the softmax warps on the same scheduler keep it busy.  So the issue
+// path is kept short: the whole warp runs the loop and its waits (the
+// operands are warp-uniform values), one lane issues, and the descriptors are
+// built once and advanced by constants: the start address sits in the low 14
 // bits in 16-B units, and shared-memory offsets below 256 KB never carry out
 // of it, so desc(addr + off) = desc(addr) + off / 16.
 static_assert(SMEM_ALLOC < (256u << 10), "descriptor arithmetic needs shared-memory offsets below 256 KB");
@@ -419,83 +444,106 @@ __device__ __forceinline__ uint64_t desc_add(uint64_t desc, uint32_t byte_off)
 template <int NT>
 __device__ void s_mma(const Params &p, Header *h, uint32_t smem, uint32_t tmem, const Unit &u)
 {
+    // The whole warp runs the loop and waits, so the operands are warp-uniform
+    // values; one lane issues each round's MMAs and commits.
+    const bool issuer = (threadIdx.x & 31) == 0;
     const uint64_t ring_desc = sdesc_sw128(smem + S_RING, 16u, 1024u);
     const uint64_t qpe_desc = sdesc_sw128(smem + S_QPE, 16u, 1024u);
     for (int t = 0; t < u.ntiles; ++t) {
         const int buf = t & 1;
-        if (t >= 2 && !wait_bar(h, smem_u32(&h->s_free[buf]), (uint32_t)((t >> 1) - 1) & 1u, p.status)) break;
+        if (t >= 2 && !warp_wait(h, smem_u32(&h->s_free[buf]), (uint32_t)((t >> 1) - 1) & 1u, p.status)) break;
         const uint32_t d = tmem + TM_S0 + 128u * (uint32_t)buf;
         bool ok = true;
 #pragma unroll 1
         for (int g = 0; g < NKR; ++g) {
-            if (!wait_bar(h, smem_u32(&h->c_full[g]), (uint32_t)t & 1u, p.status)) { ok = false; break; }
+            if (!warp_wait(h, smem_u32(&h->c_full[g]), (uint32_t)t & 1u, p.status)) { ok = false; break; }
             tc_fence_after_sync();
-            if (g == 0) {
-                // valid bits in key order: byte w = key groups w (low nibble) and w + 16 (high nibble)
-                const volatile uint8_t *src = reinterpret_cast<const volatile uint8_t *>(&h->t_valid[t & 1][0]);
-                uint64_t w0 = 0, w1 = 0;
+            const uint64_t b0 = desc_add(ring_desc, (uint32_t)g * KROUND);
+            const uint32_t a0 = tmem + 32u * (uint32_t)(g * RCHUNKS);
+            if (issuer) {
 #pragma unroll
-                for (int w = 0; w < 16; ++w) {
-                    const uint64_t v = src[w];
-                    w0 |= (v & 0xFull) << (4 * w);
-                    w1 |= ((v >> 4) & 0xFull) << (4 * w);
+                for (int cc = 0; cc < RCHUNKS; ++cc) {
+                    const uint64_t b = desc_add(b0, (uint32_t)cc * KCHUNK);
+                    if (g * RCHUNKS + cc < 8) {
+#pragma unroll
+                        for (int k = 0; k < 4; ++k)
+                            mma_ts(d, a0 + 32u * (uint32_t)cc + 8u * (uint32_t)k, desc_add(b, 32u * (uint32_t)k), IDESC_S,
+                                   (g | cc | k) ? 1u : 0u);
+                    } else {
+#pragma unroll
+                        for (int k = 0; k < 4; ++k)
+                            mma_ss(d, desc_add(qpe_desc, 32u * (uint32_t)k), desc_add(b, 32u * (uint32_t)k), IDESC_S, 1u);
+                    }
                 }
-                volatile uint64_t *dst = &h->s_valid[buf][0];
-                dst[0] = w0;
-                dst[1] = w1;
+                mma_commit_multicast(smem_u32(&h->c_empty[g]), Shape<NT>::S_MASK);   // every S CTA may refill the slot
             }
-#pragma unroll
-            for (int cc = 0; cc < RCHUNKS; ++cc) {
-                const int c = g * RCHUNKS + cc;
-                const uint64_t b = desc_add(ring_desc, (uint32_t)g * KROUND + (uint32_t)cc * KCHUNK);
-                if (c < 8) {
-#pragma unroll
-                    for (int k = 0; k < 4; ++k)
-                        mma_ts(d, tmem + 32u * (uint32_t)c + 8u * (uint32_t)k, desc_add(b, 32u * (uint32_t)k), IDESC_S,
-                               (c | k) ? 1u : 0u);
-                } else {
-#pragma unroll
-                    for (int k = 0; k < 4; ++k)
-                        mma_ss(d, desc_add(qpe_desc, 32u * (uint32_t)k), desc_add(b, 32u * (uint32_t)k), IDESC_S, 1u);
-                }
-            }
-            mma_commit_multicast(smem_u32(&h->c_empty[g]), Shape<NT>::S_MASK);   // every S CTA may refill the slot
+            __syncwarp();
         }
         if (!ok) break;
-        mma_commit(smem_u32(&h->s_full[buf]));
-        mbar_arrive(smem_u32(&h->s_full[buf]));
+        if (issuer) {
+            mma_commit(smem_u32(&h->s_full[buf]));
+            mbar_arrive(smem_u32(&h->s_full[buf]));
+        }
+        __syncwarp();
     }
-    mma_commit(smem_u32(&h->drain));
-    wait_bar(h, smem_u32(&h->drain), 0u, p.status, false, false);
+    if (issuer) mma_commit(smem_u32(&h->drain));
+    __syncwarp();
+    warp_wait(h, smem_u32(&h->drain), 0u, p.status, false, TIMEOUT_NS, false);
 }
 
 // ------------------------------------------------------------------ S role: softmax (warps 0-7)
 
-// nbits (<= 64) mask bits starting at bit index bit0 as raw bytes (loads
-// only), and their combination into a word (bit n = bit bit0 + n).
+// Valid-slot bits of softmax group `grp`'s 64 keys of tile t (bit n = key
+// 64 grp + n), from the producers' per-key-group nibbles: eight bytes, each
+// holding one nibble, are packed into 32 bits by three shift-or-mask steps.
+// The ring of four tiles is never overwritten too early: the producers write
+// tile t + 4's entry after the score MMAs of tile t + 3 began, which waited
+// for the softmax to free the score buffer of tile t + 1, so every softmax
+// thread has read tile t's entry by then.  The producers' bytes reach this
+// thread through c_full (their arrive, the MMA thread's wait) and s_full
+// (the MMA thread's arrive, this thread's wait).
+__device__ __forceinline__ uint64_t pack_nibbles(uint64_t x)
+{
+    x = (x | (x >> 4)) & 0x00FF00FF00FF00FFull;
+    x = (x | (x >> 8)) & 0x0000FFFF0000FFFFull;
+    return (x | (x >> 16)) & 0xFFFFFFFFull;
+}
+
+__device__ __forceinline__ uint64_t valid_bits(const Header *h, int t, int grp)
+{
+    const volatile uint64_t *v = reinterpret_cast<const volatile uint64_t *>(&h->t_valid[t & 3][16 * grp]);
+    return pack_nibbles(v[0]) | (pack_nibbles(v[1]) << 32);
+}
+
+
+// nbits (<= 64) mask bits starting at bit index bit0, loaded as the one or
+// two aligned 8-byte words that hold them (loads only), and their
+// combination into a word (bit n = bit bit0 + n).  An aligned word that
+// holds at least one of the wanted bytes lies in the same page as that byte,
+// so the surplus bytes it carries never reach unmapped memory.
 struct MaskBytes {
-    uint32_t b[9];
+    uint64_t w0, w1;
     int sh, nbits;
 };
 
 __device__ __forceinline__ MaskBytes load_mask(const uint8_t *mask, int64_t bit0, int nbits)
 {
     MaskBytes m;
-    m.sh = (int)(bit0 & 7);
+    m.w0 = m.w1 = 0;
     m.nbits = nbits;
-    const int64_t first = bit0 >> 3;
-    const int nb = nbits > 0 ? (int)(((bit0 + nbits - 1) >> 3) - first + 1) : 0;
-#pragma unroll
-    for (int k = 0; k < 9; ++k) m.b[k] = k < nb ? (uint32_t)__ldg(mask + first + k) : 0u;
+    const uintptr_t addr = reinterpret_cast<uintptr_t>(mask) + (uintptr_t)(bit0 >> 3);
+    const uintptr_t aligned = addr & ~(uintptr_t)7;
+    m.sh = (int)((addr - aligned) * 8 + (uintptr_t)(bit0 & 7));   // 0..63
+    if (nbits > 0) {
+        m.w0 = __ldg(reinterpret_cast<const unsigned long long *>(aligned));
+        if (m.sh + nbits > 64) m.w1 = __ldg(reinterpret_cast<const unsigned long long *>(aligned) + 1);
+    }
     return m;
 }
 
 __device__ __forceinline__ uint64_t mask_word(const MaskBytes &m)
 {
-    uint64_t lo = 0;
-#pragma unroll
-    for (int k = 0; k < 8; ++k) lo |= (uint64_t)m.b[k] << (8 * k);
-    uint64_t w = m.sh ? ((lo >> m.sh) | ((uint64_t)m.b[8] << (64 - m.sh))) : lo;
+    uint64_t w = m.sh ? ((m.w0 >> m.sh) | (m.w1 << (64 - m.sh))) : m.w0;
     if (m.nbits < 64) w &= m.nbits > 0 ? (1ull << m.nbits) - 1ull : 0ull;
     return w;
 }
@@ -585,7 +633,7 @@ __device__ void s_softmax(const Params &p, Header *h, uint32_t smem, uint32_t tm
     const uint32_t partner = 2u * (uint32_t)u.half + 1u;   // the O CTA of this row tile
     float *xmax = reinterpret_cast<float *>(reinterpret_cast<uint8_t *>(h) + S_XMAX);
     float m_used = -INFINITY, l = 0.f;
-    bool ok = true;
+    bool ok = true, slot_failed = false;
 
     // This group's mask bits of a tile: bytes loaded a tile ahead, combined after use.
     auto mask_of = [&](int t) -> MaskBytes {
@@ -604,7 +652,7 @@ __device__ void s_softmax(const Params &p, Header *h, uint32_t smem, uint32_t tm
         uint32_t sa[32], sb[32];
         tmem_ld32(s_col, sa);
         tmem_ld32(s_col + 32u, sb);
-        const uint64_t vis = *reinterpret_cast<volatile uint64_t *>(&h->s_valid[buf][grp]) & bits;
+        const uint64_t vis = valid_bits(h, t, grp) & bits;
         tmem_ld_wait();
         // The scores are in registers: the MMAs may refill this S buffer.
         tc_fence_before_sync();
@@ -629,8 +677,10 @@ __device__ void s_softmax(const Params &p, Header *h, uint32_t smem, uint32_t tm
         xmax[(buf * 2 + grp) * ROWS + r] = lmax;
         // The staging slot is free once the previous bulk copy has read it.
         if (leader) bulk_wait_read_all();
-        // Both groups: maxima exchanged, staging slots free; all agree to go on.
-        if (!named_barrier_and(5, SOFTMAX_THREADS, got)) { ok = false; break; }
+        // Both groups: maxima exchanged, staging slots free; all agree to go on
+        // (a P slot wait that gave up in either group on the previous tile
+        // votes no here, so the groups always leave the loop together).
+        if (!named_barrier_and(5, SOFTMAX_THREADS, got && !slot_failed)) { ok = false; break; }
         float mx = fmaxf(lmax, xmax[(buf * 2 + (1 - grp)) * ROWS + r]);
         mx = mx == -INFINITY ? -INFINITY : mx * sl2;   // log2 units
         float alpha = 1.f;
@@ -677,13 +727,16 @@ __device__ void s_softmax(const Params &p, Header *h, uint32_t smem, uint32_t tm
             if (lane == 0) reinterpret_cast<uint32_t *>(stage + PTILE + ROWS * 4)[quad] = any;
         }
         fence_proxy_async_smem();
-        // The partner must be done with P slot [grp][t & 1] (its use two tiles ago).
+        // The partner must be done with P slot [grp][t & 1] (its use two tiles
+        // ago).  Each group waits for its own slot and its own 128 threads'
+        // P stores; the other group does not wait for it here.
         bool slot_free = true;
         if (leader && t >= 2)
             slot_free = wait_bar(h, smem_u32(&h->p_empty[grp][buf]), (uint32_t)((t >> 1) - 1) & 1u, p.status);
-        // Both groups vote here too, so they always leave the loop together.
-        if (!named_barrier_and(6, SOFTMAX_THREADS, slot_free)) { ok = false; break; }
-        if (leader) {
+        const bool group_ok = grp == 0 ? named_barrier_and(6, SOFTMAX_THREADS / 2, slot_free)
+                                       : named_barrier_and(9, SOFTMAX_THREADS / 2, slot_free);
+        if (!group_ok) slot_failed = true;
+        if (leader && !slot_failed) {
             bulk_copy_to_cluster(map_cluster(smem + O_PSLOT + (uint32_t)(2 * grp + buf) * PSLOT, partner), stage_u32,
                                  copy_bytes, map_cluster(smem_u32(&h->p_full[grp][buf]), partner));
             bulk_commit_group();
@@ -692,6 +745,7 @@ __device__ void s_softmax(const Params &p, Header *h, uint32_t smem, uint32_t tm
         bits = mask_word(nm);
         if (t + 2 < u.ntiles) nm = mask_of(t + 2);
     }
+    if (slot_failed) ok = false;
     if (leader) bulk_wait_read_all();
 
     // Partial sums of group 1 -> group 0 (both groups always reach this barrier).
@@ -789,13 +843,15 @@ __device__ void o_gather(const Params &p, Header *h, const CUtensorMap *tmap, co
     if (!ok) settle_copies();
 }
 
-// ------------------------------------------------------------------ O role: MMA issue (warp 16, lane 0)
+// ------------------------------------------------------------------ O role: MMA issue (warp 24)
 //
 // O += P V per 64-key O tile: two halves of the value dims, N = 256 each.
 // P slot [g][par] of O tile ot: g = ot & 1 (softmax group), par = (ot >> 1) & 1.
 template <int NT>
 __device__ void o_mma(const Params &p, Header *h, uint32_t smem, uint32_t tmem, const Unit &u)
 {
+    // Run by the whole warp like s_mma: uniform operands, one issuing lane.
+    const bool issuer = (threadIdx.x & 31) == 0;
     const int nt = 2 * u.ntiles;
     const uint64_t p_desc = sdesc_sw128(smem + O_PSLOT, 16u, 1024u);   // A: P, K-major
     const uint64_t v_desc = sdesc_sw128(smem + O_VRING, VCHUNK, 1024u);  // B: V, MN-major
@@ -805,42 +861,55 @@ __device__ void o_mma(const Params &p, Header *h, uint32_t smem, uint32_t tmem, 
     bool ok = true;
     for (int ot = 0; ot < nt && ok; ++ot) {
         const int g = ot & 1, par = (ot >> 1) & 1;
-        if (!wait_bar(h, smem_u32(&h->p_full[g][par]), (pphase >> (2 * g + par)) & 1u, p.status)) { ok = false; break; }
+        if (!warp_wait(h, smem_u32(&h->p_full[g][par]), (pphase >> (2 * g + par)) & 1u, p.status)) { ok = false; break; }
         pphase ^= 1u << (2 * g + par);
         if (g == 0 && ot > 0) {
             const volatile uint32_t *f = reinterpret_cast<const volatile uint32_t *>(
                 reinterpret_cast<uint8_t *>(h) + O_PSLOT + (2 * g + par) * PSLOT + PTILE + ROWS * 4);
             if (f[0] | f[1] | f[2] | f[3]) {
-                mma_commit(smem_u32(&h->pv_sync));
-                if (!wait_bar(h, smem_u32(&h->pv_sync), nrs & 1u, p.status)) { ok = false; break; }
-                *reinterpret_cast<volatile int32_t *>(&h->rs_slot) = par;
-                mbar_arrive(smem_u32(&h->rs_req));
-                if (!wait_bar(h, smem_u32(&h->rs_done), nrs & 1u, p.status)) { ok = false; break; }
+                if (issuer) mma_commit(smem_u32(&h->pv_sync));
+                __syncwarp();
+                if (!warp_wait(h, smem_u32(&h->pv_sync), nrs & 1u, p.status)) { ok = false; break; }
+                if (issuer) {
+                    *reinterpret_cast<volatile int32_t *>(&h->rs_slot) = par;
+                    mbar_arrive(smem_u32(&h->rs_req));
+                }
+                __syncwarp();
+                if (!warp_wait(h, smem_u32(&h->rs_done), nrs & 1u, p.status)) { ok = false; break; }
                 ++nrs;
             }
         }
         tc_fence_after_sync();
+        const uint64_t a = desc_add(p_desc, (uint32_t)(2 * g + par) * PSLOT);
 #pragma unroll 1
         for (int hf = 0; hf < 2; ++hf) {
-            if (!wait_bar(h, smem_u32(&h->v_full[slot]), phase, p.status)) { ok = false; break; }
+            if (!warp_wait(h, smem_u32(&h->v_full[slot]), phase, p.status)) { ok = false; break; }
             tc_fence_after_sync();
-            const uint64_t a = desc_add(p_desc, (uint32_t)(2 * g + par) * PSLOT);
             const uint64_t b = desc_add(v_desc, (uint32_t)slot * VHALF);
+            if (issuer) {
 #pragma unroll
-            for (int k = 0; k < KEYS_O / 16; ++k)
-                mma_ss(tmem + 256u * (uint32_t)hf, desc_add(a, 32u * (uint32_t)k), desc_add(b, (uint32_t)k * 16u * 128u),
-                       IDESC_PV, (ot | k) ? 1u : 0u);
-            mma_commit_multicast(smem_u32(&h->v_empty[slot]), Shape<NT>::O_MASK);   // every O CTA may refill the slot
+                for (int k = 0; k < KEYS_O / 16; ++k)
+                    mma_ss(tmem + 256u * (uint32_t)hf, desc_add(a, 32u * (uint32_t)k),
+                           desc_add(b, (uint32_t)k * 16u * 128u), IDESC_PV, (ot | k) ? 1u : 0u);
+                mma_commit_multicast(smem_u32(&h->v_empty[slot]), Shape<NT>::O_MASK);   // every O CTA may refill the slot
+            }
+            __syncwarp();
             if (++slot == NVH) { slot = 0; phase ^= 1u; }
         }
         if (!ok) break;
-        mma_commit_multicast(smem_u32(&h->p_empty[g][par]), (uint16_t)(1u << (2 * u.half)));   // this row tile's S CTA
-        // arm this slot for its next P transfer
-        mbar_arrive_expect_tx(smem_u32(&h->p_full[g][par]), g == 0 ? PTILE + SIDE_BYTES : PTILE);
+        if (issuer) {
+            mma_commit_multicast(smem_u32(&h->p_empty[g][par]), (uint16_t)(1u << (2 * u.half)));   // this row tile's S CTA
+            // arm this slot for its next P transfer
+            mbar_arrive_expect_tx(smem_u32(&h->p_full[g][par]), g == 0 ? PTILE + SIDE_BYTES : PTILE);
+        }
+        __syncwarp();
     }
-    mma_commit(smem_u32(&h->drain));
-    *reinterpret_cast<volatile int32_t *>(&h->rs_slot) = -1;
-    mbar_arrive(smem_u32(&h->rs_req));
+    if (issuer) {
+        mma_commit(smem_u32(&h->drain));
+        *reinterpret_cast<volatile int32_t *>(&h->rs_slot) = -1;
+        mbar_arrive(smem_u32(&h->rs_req));
+    }
+    __syncwarp();
     if (!ok) settle_copies();   // P transfers already on their way land before the CTA can exit
 }
 
@@ -852,7 +921,7 @@ __device__ void o_rows(const Params &p, Header *h, uint32_t smem, uint32_t tmem,
     const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
     bool ok = true;
     for (uint32_t n = 0;; ++n) {
-        if (!warp_wait(h, smem_u32(&h->rs_req), n & 1u, p.status)) { ok = false; break; }
+        if (!__all_sync(0xffffffffu, wait_idle(h, smem_u32(&h->rs_req), n & 1u, p.status))) { ok = false; break; }
         const int par = *reinterpret_cast<volatile int32_t *>(&h->rs_slot);
         if (par < 0) break;
         const float a = reinterpret_cast<const float *>(reinterpret_cast<uint8_t *>(h) + O_PSLOT +
@@ -1027,8 +1096,8 @@ __global__ void __launch_bounds__(THREADS, 1)
             if (role == 0) {
                 named_barrier_sync(1, SOFTMAX_THREADS + 32);
                 tc_fence_after_sync();
-                if (lane == 0) s_mma<NT>(p, h, smem, tmem, u);
-            } else if (lane == 0) {
+                s_mma<NT>(p, h, smem, tmem, u);
+            } else {
                 o_mma<NT>(p, h, smem, tmem, u);
             }
         }

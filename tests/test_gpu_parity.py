@@ -177,6 +177,27 @@ def test_random_prefix_bits_and_blind_rows(impl):
     assert_parity(got, ref, f"random prefix/{impl}")
 
 
+@pytest.mark.parametrize("offset", [1, 3, 7])
+@pytest.mark.parametrize("impl", IMPLS)
+def test_mask_at_unaligned_address(impl, offset):
+    """The custom mask passed as a view that starts `offset` bytes into its
+    buffer, with random prefix bits (every row's bit offset differs): the
+    kernels read it in aligned words and shift it into place."""
+    prefix, drafts, H = [300, 77, 5], [9, 4, 2], 4
+    rng = np.random.default_rng(offset)
+    pv = [rng.random((t, l)) < 0.6 for l, t in zip(prefix, drafts)]
+    inp = W.make_inputs(prefix, drafts, H, pool_size=1024, seed=30 + offset,
+                        extra_prefix_mask=lambda b, t, l: pv[b])
+    d = device_inputs(inp)
+    n = d["custom_mask"].numel()
+    buf = torch.full((n + 16,), 0xA5, dtype=torch.uint8, device="cuda")
+    buf[offset:offset + n] = d["custom_mask"]
+    d["custom_mask"] = buf[offset:offset + n]
+    out, status = run(inp, impl=impl, num_splits=3, d=d)
+    assert status == 0
+    assert_parity(as_rows(out), oracle_rows(inp), f"mask at +{offset}/{impl}")
+
+
 @pytest.mark.parametrize("impl", IMPLS)
 def test_strided_q_and_out(impl):
     """q and out as views with padded token/head strides (no .contiguous())."""
