@@ -34,10 +34,10 @@
  *     (Decision 6: no replay-metadata hook needed).  Work is ordered on
  *     `stream` (0 = legacy default stream): when a call may hold requests
  *     of both tensor-core cluster shapes (max_q_per_req * num_heads > 128),
- *     the small requests' launch runs on a library-owned second stream,
- *     forked from `stream` by an event before it and joined back by an
- *     event before the combine, which stream capture records as a fork and
- *     a join of the graph.  Per device the library holds that stream, its
+ *     the small requests' launch runs on `stream` and the large requests'
+ *     launch on a library-owned second stream, forked from `stream` by an
+ *     event before them and joined back by an event before the combine,
+ *     which stream capture records as a fork and a join of the graph.  Per device the library holds that stream, its
  *     two events (created by verify_attn_init) and the tensor-map
  *     descriptors of the last pool it saw (host memory);
  *   - host-side argument errors are reported by a negative VA_ERR_* return
@@ -51,7 +51,7 @@
  * Thread safety: calls may be made from several host threads; concurrent
  * calls must use distinct workspaces.  Mixed-shape calls on one device share
  * the library's second stream (a lock keeps each call's fork, launch and
- * join together), so their small-request launches run one after another.
+ * join together), so their large-request launches run one after another.
  * A stream capture that has recorded a mixed-shape call holds that second
  * stream until the capture ends (the forked stream belongs to the capture):
  * on that device, make no mixed-shape call from another thread meanwhile.

@@ -664,13 +664,13 @@ __device__ void s_softmax(const Params &p, Header *h, uint32_t smem, uint32_t tm
         float mx4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};   // independent chains
         if (all_vis) {
 #pragma unroll
-            for (int n = 0; n < 32; ++n) mx4[n & 3] = fmaxf(mx4[n & 3], fmaxf(__uint_as_float(sa[n]), __uint_as_float(sb[n])));
+            for (int n = 0; n < 32; ++n) mx4[n & 3] = max3f(mx4[n & 3], __uint_as_float(sa[n]), __uint_as_float(sb[n]));
         } else {
 #pragma unroll
             for (int n = 0; n < 32; ++n) {
                 const float a = ((v0 >> n) & 1u) ? __uint_as_float(sa[n]) : -INFINITY;
                 const float b = ((v1 >> n) & 1u) ? __uint_as_float(sb[n]) : -INFINITY;
-                mx4[n & 3] = fmaxf(mx4[n & 3], fmaxf(a, b));
+                mx4[n & 3] = max3f(mx4[n & 3], a, b);
             }
         }
         const float lmax = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3]));
@@ -694,9 +694,11 @@ __device__ void s_softmax(const Params &p, Header *h, uint32_t smem, uint32_t tm
             rescale = true;
         }
 
-        // p = 2^(s * sl2 - m_used) for this group's 64 keys; masked keys give 0.
+        // p = 2^(s * sl2 - m_used) for this group's 64 keys; masked keys give
+        // 0.  Scaling and summing run on key pairs (packed fp32 FMA and add).
         const float neg_m = m_used == -INFINITY ? 0.f : -m_used;
-        float ps4[4] = {0.f, 0.f, 0.f, 0.f};   // independent chains
+        const uint64_t sl2x2 = f2_pack(sl2, sl2), negm2 = f2_pack(neg_m, neg_m);
+        uint64_t ps2[4] = {0ull, 0ull, 0ull, 0ull};   // independent chains of pair sums (+0.0f bits)
 #pragma unroll
         for (int part = 0; part < 2; ++part) {
             const uint32_t *sv = part ? sb : sa;
@@ -704,13 +706,16 @@ __device__ void s_softmax(const Params &p, Header *h, uint32_t smem, uint32_t tm
             uint32_t pk[16];
 #pragma unroll
             for (int n = 0; n < 16; ++n) {
-                float p0 = ex2_approx(fmaf(__uint_as_float(sv[2 * n]), sl2, neg_m));
-                float p1 = ex2_approx(fmaf(__uint_as_float(sv[2 * n + 1]), sl2, neg_m));
+                float x0, x1;
+                f2_unpack(f2_fma(f2_pack(__uint_as_float(sv[2 * n]), __uint_as_float(sv[2 * n + 1])), sl2x2, negm2),
+                          x0, x1);
+                float p0 = ex2_approx(x0);
+                float p1 = ex2_approx(x1);
                 if (!all_vis) {
                     p0 = ((vq >> (2 * n)) & 1u) ? p0 : 0.f;
                     p1 = ((vq >> (2 * n + 1)) & 1u) ? p1 : 0.f;
                 }
-                ps4[n & 3] += p0 + p1;
+                ps2[n & 3] = f2_add(ps2[n & 3], f2_pack(p0, p1));
                 pk[n] = pack_bf16x2(p0, p1);
             }
             // keys 32*part .. +31 of this half: 16-B pieces 4*part .. 4*part+3 of row r
@@ -719,7 +724,11 @@ __device__ void s_softmax(const Params &p, Header *h, uint32_t smem, uint32_t tm
                 *reinterpret_cast<uint4 *>(prow + ((((uint32_t)(4 * part + qq)) ^ (uint32_t)(r & 7)) << 4)) =
                     make_uint4(pk[4 * qq], pk[4 * qq + 1], pk[4 * qq + 2], pk[4 * qq + 3]);
         }
-        l += (ps4[0] + ps4[1]) + (ps4[2] + ps4[3]);
+        {
+            float a0, a1;
+            f2_unpack(f2_add(f2_add(ps2[0], ps2[1]), f2_add(ps2[2], ps2[3])), a0, a1);
+            l += a0 + a1;
+        }
         if (grp == 0) {
             // The first half's O tile rescales O; the second half follows with the same maximum.
             reinterpret_cast<float *>(stage + PTILE)[r] = rescale ? alpha : 1.f;
@@ -1192,7 +1201,7 @@ cudaError_t launch_shape(const Params &p, const CUtensorMap &map, const CUtensor
     return cudaLaunchKernelEx(&cfg, tc_split_kernel<NT>, p, map, run_k, run_v);
 }
 
-// Per device: a second stream and the two events that fork the 2-CTA launch
+// Per device: a second stream and the two events that fork the 4-CTA launch
 // of a mixed call onto it and join it back (created once, before capture).
 struct SideStream {
     cudaStream_t stream = nullptr;
@@ -1264,16 +1273,20 @@ cudaError_t launch_tc_split(const Params &p, cudaStream_t stream)
     Params big = p, small = p;
     big.rows_lo = ROWS;
     small.rows_hi = ROWS;
-    // The small requests' grid goes first: its clusters take SMs before the
-    // large grid fills the GPU, so short units do not end up in the tail
+    // The small requests' grid must start first: its clusters take SMs before
+    // the large grid fills the GPU, so short units do not end up in the tail
     // (measured: 635 against 671 us per graph replay of the ragged workload).
+    // So it goes on the caller's stream, where it depends on nothing new, and
+    // the large grid on the side stream behind the fork event; the other way
+    // round the large grid started first in direct calls, whatever the
+    // enqueue order.
     std::lock_guard<std::mutex> g(ss.lock);
     cudaError_t e;
     if ((e = cudaEventRecord(ss.fork, stream)) != cudaSuccess) return e;
+    if ((e = launch_shape<1>(small, map, run_k, run_v, stream, 1)) != cudaSuccess) return e;
     if ((e = cudaStreamWaitEvent(ss.stream, ss.fork, 0)) != cudaSuccess) return e;
-    if ((e = launch_shape<1>(small, map, run_k, run_v, ss.stream, 1)) != cudaSuccess) return e;
+    if ((e = launch_shape<2>(big, map, run_k, run_v, ss.stream)) != cudaSuccess) return e;
     if ((e = cudaEventRecord(ss.join, ss.stream)) != cudaSuccess) return e;
-    if ((e = launch_shape<2>(big, map, run_k, run_v, stream)) != cudaSuccess) return e;
     return cudaStreamWaitEvent(stream, ss.join, 0);
 }
 
