@@ -699,24 +699,28 @@ __device__ void s_softmax(const Params &p, Header *h, uint32_t smem, uint32_t tm
         const float neg_m = m_used == -INFINITY ? 0.f : -m_used;
         const uint64_t sl2x2 = f2_pack(sl2, sl2), negm2 = f2_pack(neg_m, neg_m);
         uint64_t ps2[4] = {0ull, 0ull, 0ull, 0ull};   // independent chains of pair sums (+0.0f bits)
+        // Per 32 keys: all scalings first, then all exponentials back to back,
+        // then sums and bf16 packing (more independent work per warp).
 #pragma unroll
         for (int part = 0; part < 2; ++part) {
             const uint32_t *sv = part ? sb : sa;
             const uint32_t vq = part ? v1 : v0;
+            float x[32];
+#pragma unroll
+            for (int n = 0; n < 16; ++n)
+                f2_unpack(f2_fma(f2_pack(__uint_as_float(sv[2 * n]), __uint_as_float(sv[2 * n + 1])), sl2x2, negm2),
+                          x[2 * n], x[2 * n + 1]);
+#pragma unroll
+            for (int n = 0; n < 32; ++n) x[n] = ex2_approx(x[n]);
+            if (!all_vis) {
+#pragma unroll
+                for (int n = 0; n < 32; ++n) x[n] = ((vq >> n) & 1u) ? x[n] : 0.f;
+            }
             uint32_t pk[16];
 #pragma unroll
             for (int n = 0; n < 16; ++n) {
-                float x0, x1;
-                f2_unpack(f2_fma(f2_pack(__uint_as_float(sv[2 * n]), __uint_as_float(sv[2 * n + 1])), sl2x2, negm2),
-                          x0, x1);
-                float p0 = ex2_approx(x0);
-                float p1 = ex2_approx(x1);
-                if (!all_vis) {
-                    p0 = ((vq >> (2 * n)) & 1u) ? p0 : 0.f;
-                    p1 = ((vq >> (2 * n + 1)) & 1u) ? p1 : 0.f;
-                }
-                ps2[n & 3] = f2_add(ps2[n & 3], f2_pack(p0, p1));
-                pk[n] = pack_bf16x2(p0, p1);
+                ps2[n & 3] = f2_add(ps2[n & 3], f2_pack(x[2 * n], x[2 * n + 1]));
+                pk[n] = pack_bf16x2(x[2 * n], x[2 * n + 1]);
             }
             // keys 32*part .. +31 of this half: 16-B pieces 4*part .. 4*part+3 of row r
 #pragma unroll
