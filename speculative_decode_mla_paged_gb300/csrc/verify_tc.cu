@@ -699,28 +699,33 @@ __device__ void s_softmax(const Params &p, Header *h, uint32_t smem, uint32_t tm
         const float neg_m = m_used == -INFINITY ? 0.f : -m_used;
         const uint64_t sl2x2 = f2_pack(sl2, sl2), negm2 = f2_pack(neg_m, neg_m);
         uint64_t ps2[4] = {0ull, 0ull, 0ull, 0ull};   // independent chains of pair sums (+0.0f bits)
-        // Per 32 keys: all scalings first, then all exponentials back to back,
-        // then sums and bf16 packing (more independent work per warp).
+        // All 64 scalings first, then all 64 exponentials back to back, then
+        // sums and bf16 packing (more independent work per warp).
+        float x[64];
+#pragma unroll
+        for (int n = 0; n < 16; ++n) {
+            f2_unpack(f2_fma(f2_pack(__uint_as_float(sa[2 * n]), __uint_as_float(sa[2 * n + 1])), sl2x2, negm2),
+                      x[2 * n], x[2 * n + 1]);
+            f2_unpack(f2_fma(f2_pack(__uint_as_float(sb[2 * n]), __uint_as_float(sb[2 * n + 1])), sl2x2, negm2),
+                      x[32 + 2 * n], x[32 + 2 * n + 1]);
+        }
+#pragma unroll
+        for (int n = 0; n < 64; ++n) x[n] = ex2_approx(x[n]);
+        if (!all_vis) {
+#pragma unroll
+            for (int n = 0; n < 32; ++n) {
+                x[n] = ((v0 >> n) & 1u) ? x[n] : 0.f;
+                x[32 + n] = ((v1 >> n) & 1u) ? x[32 + n] : 0.f;
+            }
+        }
 #pragma unroll
         for (int part = 0; part < 2; ++part) {
-            const uint32_t *sv = part ? sb : sa;
-            const uint32_t vq = part ? v1 : v0;
-            float x[32];
-#pragma unroll
-            for (int n = 0; n < 16; ++n)
-                f2_unpack(f2_fma(f2_pack(__uint_as_float(sv[2 * n]), __uint_as_float(sv[2 * n + 1])), sl2x2, negm2),
-                          x[2 * n], x[2 * n + 1]);
-#pragma unroll
-            for (int n = 0; n < 32; ++n) x[n] = ex2_approx(x[n]);
-            if (!all_vis) {
-#pragma unroll
-                for (int n = 0; n < 32; ++n) x[n] = ((vq >> n) & 1u) ? x[n] : 0.f;
-            }
             uint32_t pk[16];
 #pragma unroll
             for (int n = 0; n < 16; ++n) {
-                ps2[n & 3] = f2_add(ps2[n & 3], f2_pack(x[2 * n], x[2 * n + 1]));
-                pk[n] = pack_bf16x2(x[2 * n], x[2 * n + 1]);
+                const float p0 = x[32 * part + 2 * n], p1 = x[32 * part + 2 * n + 1];
+                ps2[n & 3] = f2_add(ps2[n & 3], f2_pack(p0, p1));
+                pk[n] = pack_bf16x2(p0, p1);
             }
             // keys 32*part .. +31 of this half: 16-B pieces 4*part .. 4*part+3 of row r
 #pragma unroll
