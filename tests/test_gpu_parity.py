@@ -1,5 +1,6 @@
 """GPU parity: the CUDA path (through the C ABI) against the CPU oracle."""
 
+import copy
 import numpy as np
 import pytest
 import torch
@@ -233,6 +234,34 @@ def test_bad_slot_sets_status_without_fault(impl):
     out, status = run(inp, impl=impl, num_splits=2)
     assert status & api.STATUS_BAD_SLOT
     assert np.all(np.isfinite(as_rows(out)))
+
+
+@pytest.mark.parametrize("impl", IMPLS)
+@pytest.mark.parametrize("drafts", [(12, 3), (40, 20)], ids=["one_row_tile", "two_row_tiles"])
+def test_bad_slots_across_many_tiles_are_skipped(drafts, impl):
+    """Slots outside the pool at scattered key positions of a 25-tile unit
+    (one split, so the per-tile valid-key bits wrap their ring many times):
+    the call sets VA_STATUS_BAD_SLOT and every row equals the oracle run on
+    the same inputs with those keys hidden from every row (the kernels skip
+    a key whose slot is invalid)."""
+    prefix, H = [3100, 700], 8
+    inp = W.make_inputs(prefix, list(drafts), H, pool_size=8192, seed=27)
+    rng = np.random.default_rng(27)
+    bad = {0: np.sort(rng.choice(prefix[0], 40, replace=False)), 1: np.array([0, 127, 128, 699])}
+    bits = np.unpackbits(inp.custom_mask, bitorder="little")[: int(inp.mask_indptr[-1])].copy()
+    kv_bad = inp.kv_indices.copy()
+    for b, keys in bad.items():
+        n = prefix[b] + drafts[b]
+        rows = bits[int(inp.mask_indptr[b]): int(inp.mask_indptr[b + 1])].reshape(drafts[b], n)
+        rows[:, keys] = 0                       # the reference: these keys hidden from every row
+        kv_bad[inp.kv_indptr[b] + keys] = inp.pool_size + 7 + keys
+    ref_inp = copy.copy(inp)
+    ref_inp.custom_mask = np.packbits(bits, bitorder="little")
+    ref = oracle_rows(ref_inp)                  # valid slots, hidden keys
+    inp.kv_indices = kv_bad                     # the kernels see the invalid slots, full mask
+    out, status = run(inp, impl=impl, num_splits=1)
+    assert status & api.STATUS_BAD_SLOT
+    assert_parity(as_rows(out), ref, f"bad slots/{impl}/{drafts}")
 
 
 @pytest.mark.parametrize("impl", IMPLS)
