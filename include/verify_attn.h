@@ -49,15 +49,16 @@
  *     reads it after its own synchronisation.
  *
  * Thread safety: calls may be made from several host threads; concurrent
- * calls must use distinct workspaces.  Mixed-shape calls on one device share
- * the library's second stream (a lock keeps each call's fork, launch and
- * join together), so their large-request launches run one after another.
- * A stream capture that has recorded a mixed-shape call holds that second
- * stream until the capture ends (the forked stream belongs to the capture):
- * on that device, make no mixed-shape call from another thread meanwhile.
- * Such a call is not supported.  Its fork would wait from a capturing
- * stream on an event recorded outside the capture, so the call can fail
- * with VA_ERR_LAUNCH and invalidate the capture.
+ * calls must use distinct workspaces.  A mixed-shape call launches its
+ * large requests on a second stream that belongs to the calling host thread
+ * (one per thread and device, created by that thread's first
+ * verify_attn_init or mixed call), so calls and stream captures made from
+ * different threads never share it, and their launches may overlap.  Within
+ * one thread, a stream capture that has recorded a mixed-shape call holds
+ * that thread's second stream until the capture ends (the forked stream
+ * belongs to the capture): make no mixed-shape call on another stream from
+ * the same thread meanwhile (its fork would wait on an event recorded in
+ * the capture, and the call can fail with VA_ERR_LAUNCH).
  */
 #ifndef VERIFY_ATTN_H
 #define VERIFY_ATTN_H
@@ -120,7 +121,9 @@ VERIFY_ATTN_API size_t verify_attn_workspace_size(int batch, int max_q_per_req, 
 
 /*
  * One-time per-device setup for the current device: kernel attributes such
- * as the dynamic shared-memory limit, the side stream and its events, and
+ * as the dynamic shared-memory limit, the calling thread's second stream and
+ * its events (each host thread that captures mixed-shape calls should call
+ * it once before capturing), and
  * the loading of the module that holds verify_attn_run_static's 32 MiB
  * array (which commits that memory).  Every entry point calls it lazily,
  * but callers that capture CUDA graphs should call it once before
@@ -251,8 +254,9 @@ VERIFY_ATTN_API int verify_attn_run_profiled(int impl, void *const *events,
  * streams at once -- race on that array, so serialise them.  The status word
  * of the last call is readable through verify_attn_static_status_word().
  *
- * The library's per-device state (this array's module, the side stream and
- * events, the tensor-map cache) belongs to the device's primary context:
+ * The library's per-device state (this array's module, the per-thread
+ * second streams and events, the tensor-map cache) belongs to the device's
+ * primary context:
  * after cudaDeviceReset, or under another context, it is not valid.
  *
  * Arguments, layouts and the other return codes are those of

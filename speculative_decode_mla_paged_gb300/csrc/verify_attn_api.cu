@@ -18,6 +18,7 @@ static_assert(va::STATUS_BAD_SLOT == VA_STATUS_BAD_SLOT && va::STATUS_BAD_META =
 namespace va {
 
 cudaError_t tc_init();
+cudaError_t tc_thread_init();
 cudaError_t launch_tc_split(const Params &p, cudaStream_t stream);
 bool tc_supported(const Params &p);
 int static_scratch_setup();   // verify_attn_static.cu
@@ -177,7 +178,13 @@ size_t verify_attn_workspace_size(int batch, int max_q_per_req, int num_heads, i
     return va::ws_size(batch, max_q_per_req, num_heads, num_splits);
 }
 
-int verify_attn_init(void) { return va::ensure_init(); }
+int verify_attn_init(void)
+{
+    const int rc = va::ensure_init();
+    if (rc != VA_OK) return rc;
+    // the calling thread's second stream, made here rather than inside a capture
+    return va::tc_thread_init() == cudaSuccess ? VA_OK : VA_ERR_LAUNCH;
+}
 
 int verify_attn_run(const void *q, int64_t q_stride_tok, int64_t q_stride_head, const void *kv_pool,
                     int64_t pool_size, const int32_t *qo_indptr, const int32_t *kv_indptr,

@@ -1181,6 +1181,8 @@ cudaError_t tc_init()
 
 bool tc_supported(const Params &p) { return p.pool_size < ((int64_t)1 << 31); }
 
+cudaError_t tc_thread_init() { return side_init(); }
+
 cudaError_t launch_wait_probe(unsigned *status, uint64_t limit_ns, cudaStream_t stream)
 {
     wait_probe_kernel<<<1, 32, 0, stream>>>(status, limit_ns);
@@ -1212,12 +1214,15 @@ cudaError_t launch_shape(const Params &p, const CUtensorMap &map, const CUtensor
 
 // Per device: a second stream and the two events that fork the 4-CTA launch
 // of a mixed call onto it and join it back (created once, before capture).
+// The second stream of mixed-shape calls, with its fork and join events:
+// one per host thread and device, so that calls (and stream captures) made
+// from different threads never share it.  A thread's calls are sequential,
+// so it needs no lock; the objects live until the process ends.
 struct SideStream {
     cudaStream_t stream = nullptr;
     cudaEvent_t fork = nullptr, join = nullptr;
-    std::mutex lock;
 };
-SideStream g_side[64];
+thread_local SideStream t_side[64];
 
 cudaError_t side_init()
 {
@@ -1225,11 +1230,12 @@ cudaError_t side_init()
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-    SideStream &ss = g_side[dev];
-    std::lock_guard<std::mutex> g(ss.lock);
-    if (ss.stream != nullptr) return cudaSuccess;
-    if ((e = cudaStreamCreateWithFlags(&ss.stream, cudaStreamNonBlocking)) != cudaSuccess) return e;
-    if ((e = cudaEventCreateWithFlags(&ss.fork, cudaEventDisableTiming)) != cudaSuccess) return e;
+    SideStream &ss = t_side[dev];
+    if (ss.join != nullptr) return cudaSuccess;
+    if (ss.stream == nullptr && (e = cudaStreamCreateWithFlags(&ss.stream, cudaStreamNonBlocking)) != cudaSuccess)
+        return e;
+    if (ss.fork == nullptr && (e = cudaEventCreateWithFlags(&ss.fork, cudaEventDisableTiming)) != cudaSuccess)
+        return e;
     return cudaEventCreateWithFlags(&ss.join, cudaEventDisableTiming);
 }
 
@@ -1276,9 +1282,10 @@ cudaError_t launch_tc_split(const Params &p, cudaStream_t stream)
     if (p.max_q_per_req * (int64_t)p.num_heads <= ROWS) return launch_shape<1>(p, map, run_k, run_v, stream);
     if (p.max_q_per_req < 1 || p.num_heads > ROWS) return launch_shape<2>(p, map, run_k, run_v, stream);
     int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64 || g_side[dev].stream == nullptr)
-        return cudaErrorNotReady;
-    SideStream &ss = g_side[dev];
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    cudaError_t e = side_init();   // this thread's first mixed call on the device creates its second stream
+    if (e != cudaSuccess) return e;
+    SideStream &ss = t_side[dev];
     Params big = p, small = p;
     big.rows_lo = ROWS;
     small.rows_hi = ROWS;
@@ -1289,8 +1296,6 @@ cudaError_t launch_tc_split(const Params &p, cudaStream_t stream)
     // the large grid on the side stream behind the fork event; the other way
     // round the large grid started first in direct calls, whatever the
     // enqueue order.
-    std::lock_guard<std::mutex> g(ss.lock);
-    cudaError_t e;
     if ((e = cudaEventRecord(ss.fork, stream)) != cudaSuccess) return e;
     if ((e = launch_shape<1>(small, map, run_k, run_v, stream, 1)) != cudaSuccess) return e;
     if ((e = cudaStreamWaitEvent(ss.stream, ss.fork, 0)) != cudaSuccess) return e;

@@ -435,8 +435,8 @@ def test_profiled_call_times_every_graph_replay():
 
 def test_concurrent_mixed_calls_from_two_threads():
     """Two host threads, each with its own workspace and stream, issue mixed
-    calls (both cluster shapes, so both go through the library's shared second
-    stream and its lock) at the same time; every output matches the oracle."""
+    calls (both cluster shapes, each forking to its thread's second stream)
+    at the same time; every output matches the oracle."""
     import threading
 
     cases = [W.make_inputs([900, 200, 40], [24, 8, 16], 8, 8192, seed=81),
@@ -461,6 +461,55 @@ def test_concurrent_mixed_calls_from_two_threads():
                 assert runner.status() == 0
                 assert_parity(as_rows(out), refs[k], f"thread {k}")
         except Exception as e:          # reported in the main thread
+            errors.append(e)
+
+    threads = [threading.Thread(target=worker, args=(k,)) for k in range(2)]
+    for t in threads:
+        t.start()
+    for t in threads:
+        t.join()
+    assert not errors, errors
+
+
+def test_concurrent_captures_of_mixed_calls_from_two_threads():
+    """Two host threads capture a mixed call (both cluster shapes, so both
+    fork to a second stream) into CUDA graphs at the same time; each thread's
+    call forks to its own second stream, so neither capture invalidates the
+    other, and every replay matches the oracle."""
+    import threading
+
+    cases = [W.make_inputs([900, 200, 40], [24, 8, 16], 8, 8192, seed=83),
+             W.make_inputs([300, 1200], [8, 32], 8, 8192, seed=84)]
+    refs = [oracle_rows(c) for c in cases]
+    devs = [device_inputs(c) for c in cases]
+    torch.cuda.synchronize()
+    both_capturing = threading.Barrier(2, timeout=60)
+    errors = []
+
+    def worker(k):
+        try:
+            c, d = cases[k], devs[k]
+            runner = api.VerifyAttention(c.batch, c.max_q_per_req, c.num_heads, 4)   # this thread's second stream
+            s = torch.cuda.Stream()
+            out = torch.zeros(c.total_q, c.num_heads, 512, dtype=torch.bfloat16, device="cuda")
+            args = (d["q"], d["kv_pool"], d["qo_indptr"], d["kv_indptr"], d["kv_indices"], d["out_cache_loc"],
+                    d["custom_mask"], d["mask_indptr"], c.sm_scale, out)
+            with torch.cuda.stream(s):
+                runner(*args)                  # warm-up outside the capture
+            s.synchronize()
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=s, capture_error_mode="thread_local"):
+                runner(*args)
+                both_capturing.wait()          # the other thread's capture is open too
+            for _ in range(3):
+                with torch.cuda.stream(s):
+                    out.zero_()
+                    g.replay()
+                s.synchronize()
+                assert runner.status() == 0
+                assert_parity(as_rows(out), refs[k], f"thread {k}")
+        except Exception as e:          # reported in the main thread
+            both_capturing.abort()
             errors.append(e)
 
     threads = [threading.Thread(target=worker, args=(k,)) for k in range(2)]
